@@ -1,0 +1,423 @@
+"""Benchmark: paged decode attention KV GB/s (+ prefill TFLOP/s) on GB300.
+
+One step = the decode hot path over one batch of the batched-decode workload
+(256 sequences, context_lens uniform in [512, 4096], 16 q / 8 kv heads,
+head_dim 128, block_size 256, 8192-block pool with shuffled block tables):
+pkv_store_kvcache of the 256 new tokens, then pkv_decode (split-KV, merge in
+the same launch). ``value`` = live K/V bytes read by the decode (each live
+element once) / step time, inputs resident in HBM (2.4 GB of K/V per step,
+larger than L2).
+
+Also reported on the same line:
+  roofline      decode kernel: algorithmic bytes / its CUDA-event time vs the
+                measured HBM copy bandwidth (MEASURED_PEAKS.json)
+  e2e           the same metric through the C ABI with host buffers: pinned
+                inputs copied in, result copied out, inside the timed region
+  prefill       varlen prefill (64 prompts, 100..1024 tokens, <=16384 per call)
+                and prefix-cached prefill (128 seqs x 1024-token shared prefix
+                + 64..512 suffix): TFLOP/s of causally live pairs, vs the
+                measured bf16 dense peak; store GB/s at prefill size
+  cpu_baseline  the oracle (fp64 C, OpenMP) on a bounded sample, host cores
+
+``--impl reference`` times the oracle itself as the reference arm.
+Multi-GPU: replicas only (the path has no exchange step); each rank runs the
+same workload on its own GPU and value sums over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attn KV GB/s & prefill attn TFLOPS (1xGB300, % roofline)"
+UNIT = "GB/s"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _src_hash(name):
+    with open(os.path.join(ROOT, "paged_kv_cache_kvh_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel_file, units_now):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None). Scaled by units processed
+    when the capture used a smaller case of the same kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_file)
+    if not e or e.get("src_sha") != _src_hash(kernel_file):
+        return None
+    return e["dram_bytes_per_launch"] * (units_now / e["units"]) if e.get("units") else e["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        self.index = index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _flush_l2(buf):
+    buf.zero_()
+
+
+# ---------------------------------------------------------------------------
+# the decode step (ours)
+# ---------------------------------------------------------------------------
+
+def decode_case(pkv, dev, seed=2):
+    wl = W.batched_decode(seed=seed)
+    gen = W.make_generator(seed, dev)
+    shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+    kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
+    B = len(wl.seqs)
+    qkv, q, k, v = W.fused_qkv(B, gen, dev)
+    meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE, table_width=W.MAX_MODEL_LEN // W.BLOCK_SIZE)
+    c = dict(wl=wl, kc=kc, vc=vc, qkv=qkv, q=q, k=k, v=v, meta=meta, B=B,
+             slot=torch.from_numpy(meta["slot_mapping"]).to(dev),
+             ctx=torch.from_numpy(meta["context_lens"]).to(dev),
+             bt=torch.from_numpy(meta["block_tables"]).to(dev),
+             ws=pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev),
+             out=torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev))
+    ctx = meta["context_lens"].astype(np.int64)
+    c["kv_bytes"] = int(ctx.sum()) * W.HKV * W.HEAD_DIM * 2 * 2
+    c["decode_alg_bytes"] = (c["kv_bytes"] + B * W.HQ * W.HEAD_DIM * 2 * 2 + meta["block_tables"].nbytes
+                             + B * 4)
+    return c
+
+
+def run_ours(args, rank, world, dev):
+    import paged_kv_cache_kvh_gb300 as pkv
+
+    c = decode_case(pkv, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        pkv.pkv_store_kvcache(c["k"], c["v"], c["kc"], c["vc"], c["slot"])
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.pkv_decode(c["q"], c["kc"], c["vc"], c["bt"], c["ctx"], W.MAX_MODEL_LEN, W.SCALE, c["ws"],
+                       out=c["out"])
+        if ev is not None:
+            ev[1].record(stream)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_total = t0.elapsed_time(t1)
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    err = pkv.pkv_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after the timed region")
+
+    # ---- e2e: host buffers through the C ABI ----
+    e2e = run_e2e(pkv, c, args, dev)
+
+    hbm, bf16, bf16_sus, src = _peaks()
+    ach = c["decode_alg_bytes"] / (dec_ms * 1e-3) / 1e9
+    roof = {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(ach / hbm, 4), "peak_source": f"{src} (hbm copy)",
+            "alg_bytes_per_launch": c["decode_alg_bytes"], "avg_launch_ms": round(dec_ms, 5),
+            "traffic": _traffic("decode.cu", c["kv_bytes"])}
+    res = {"metric": METRIC, "value": round(world * c["kv_bytes"] / (ms_step * 1e-3) / 1e9, 1), "unit": UNIT,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
+           "config": {"workload": "batched_decode_b256_ctx512-4096: store_kvcache(256 tokens) + GQA decode",
+                      "num_seqs": c["B"], "q_heads": W.HQ, "kv_heads": W.HKV, "head_dim": W.HEAD_DIM,
+                      "block_size": W.BLOCK_SIZE, "num_blocks": c["wl"].num_blocks,
+                      "sum_context_lens": int(c["meta"]["context_lens"].sum()),
+                      "kv_bytes_per_step": c["kv_bytes"],
+                      "l2": "inputs larger than L2 (2.4 GB of live K/V read per step)",
+                      "parallelism": f"replicas x{world}"},
+           "roofline": roof, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
+    if rank == 0 and not args.no_prefill:
+        res["prefill"] = run_prefill(pkv, args, dev, bf16)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(c, budget_s=args.cpu_seconds)
+    return res
+
+
+def run_e2e(pkv, c, args, dev):
+    B = c["B"]
+    hq = c["q"].contiguous().cpu().pin_memory()
+    hk = c["k"].contiguous().cpu().pin_memory()
+    hv = c["v"].contiguous().cpu().pin_memory()
+    hslot = torch.from_numpy(c["meta"]["slot_mapping"]).pin_memory()
+    hctx = torch.from_numpy(c["meta"]["context_lens"]).pin_memory()
+    hbt = torch.from_numpy(c["meta"]["block_tables"]).pin_memory()
+    hout = torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16).pin_memory()
+    dq, dk, dv = torch.empty_like(c["q"].contiguous()), torch.empty_like(c["k"].contiguous()), \
+        torch.empty_like(c["v"].contiguous())
+    dslot, dctx, dbt = torch.empty_like(c["slot"]), torch.empty_like(c["ctx"]), torch.empty_like(c["bt"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for d, h in ((dq, hq), (dk, hk), (dv, hv), (dslot, hslot), (dctx, hctx), (dbt, hbt)):
+            d.copy_(h, non_blocking=True)
+        pkv.pkv_store_kvcache(dk, dv, c["kc"], c["vc"], dslot)
+        pkv.pkv_decode(dq, c["kc"], c["vc"], dbt, dctx, W.MAX_MODEL_LEN, W.SCALE, c["ws"], out=c["out"])
+        hout.copy_(c["out"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hslot, hctx, hbt))
+    return {"value": round(c["kv_bytes"] / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * hout.element_size()}
+
+
+def _prefill_flops(seqs):
+    tot = 0
+    for s in seqs:
+        lq, lk = s.num_scheduled_tokens, s.num_cached_tokens + s.num_scheduled_tokens
+        # sum over query rows of (position + 1) live keys
+        tot += lq * (lk - lq) + lq * (lq + 1) // 2
+    return 4 * W.HEAD_DIM * W.HQ * tot
+
+
+def run_prefill(pkv, args, dev, bf16_peak):
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    iters = max(3, min(args.steps, 20))
+    for name, wl in (("varlen_prefill_64p_len100-1024", W.varlen_prefill()),
+                     ("prefix_prefill_128s_prefix1024_suffix64-512", W.prefix_prefill())):
+        gen = W.make_generator(wl.seed, dev)
+        shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+        kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
+        calls = []
+        for seqs in wl.seqs:
+            T = sum(s.num_scheduled_tokens for s in seqs)
+            _, q, k, v = W.fused_qkv(T, gen, dev)
+            m = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
+            calls.append(dict(q=q, k=k, v=v, m=m, T=T, flops=_prefill_flops(seqs),
+                              slot=torch.from_numpy(m["slot_mapping"]).to(dev),
+                              cq=torch.from_numpy(m["cu_seqlens_q"]).to(dev),
+                              ck=torch.from_numpy(m["cu_seqlens_k"]).to(dev),
+                              bt=torch.from_numpy(m["block_tables"]).to(dev)))
+        pre_ms, st_ms = [], []
+        for it in range(iters + 3):
+            for cl in calls:
+                _flush_l2(flush)
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record()
+                pkv.pkv_store_kvcache(cl["k"], cl["v"], kc, vc, cl["slot"])
+                e1.record()
+                pkv.pkv_prefill_varlen(cl["q"], cl["cq"], cl["ck"], cl["m"]["max_seqlen_q"], cl["m"]["max_seqlen_k"],
+                                       W.SCALE, k_cache=kc, v_cache=vc, block_tables=cl["bt"])
+                e2.record()
+                if it >= 3:
+                    cl.setdefault("ev", []).append((e0, e1, e2))
+        torch.cuda.synchronize()
+        flops = sum(cl["flops"] for cl in calls)
+        t_pre = sum(e1.elapsed_time(e2) for cl in calls for (_, e1, e2) in cl["ev"]) / iters
+        t_st = sum(e0.elapsed_time(e1) for cl in calls for (e0, e1, _) in cl["ev"]) / iters
+        store_bytes = sum(4 * int((cl["m"]["slot_mapping"] >= 0).sum()) * W.HKV * W.HEAD_DIM * 2 for cl in calls)
+        tf = flops / (t_pre * 1e-3) / 1e12
+        res[name] = {"calls": len(calls), "tokens": sum(cl["T"] for cl in calls), "gflop": round(flops / 1e9, 2),
+                     "prefill_ms": round(t_pre, 4), "tflops": round(tf, 1),
+                     "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(tf, 1),
+                                  "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
+                                  "peak_source": "measured bf16 dense (cuBLAS burst)",
+                                  "traffic": _traffic("prefill.cu", flops)},
+                     "store_ms": round(t_st, 4), "store_gbs": round(store_bytes / (t_st * 1e-3) / 1e9, 1),
+                     "l2": "256 MB buffer written between launches"}
+    assert pkv.pkv_device_error() == 0
+    return res
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU) arm
+# ---------------------------------------------------------------------------
+
+def _oracle_sample(num_sample, seed=2):
+    """The first num_sample sequences of the batched-decode workload, their
+    blocks generated on the host (compact pool), for the oracle."""
+    import oracle
+    wl = W.batched_decode(seed=seed)
+    seqs = wl.seqs[:num_sample]
+    used = sorted({b for s in seqs for b in s.block_table})
+    remap = {b: i for i, b in enumerate(used)}
+    gen = W.make_generator(seed, "cpu")
+    shape = (len(used), W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)  # noqa: E731
+    kc, vc = bits(W.normal_bf16(shape, gen, "cpu")), bits(W.normal_bf16(shape, gen, "cpu"))
+    _, q, k, v = W.fused_qkv(num_sample, gen, "cpu")
+    osq = [oracle.SeqState(s.num_tokens, [remap[b] for b in s.block_table]) for s in seqs]
+    m = oracle.prepare_decode(osq, W.BLOCK_SIZE)
+    kv_bytes = int(m["context_lens"].astype(np.int64).sum()) * W.HKV * W.HEAD_DIM * 4
+    return dict(q=bits(q), k=bits(k), v=bits(v), kc=kc, vc=vc, m=m, kv_bytes=kv_bytes, n=num_sample)
+
+
+def _oracle_step(orc, s):
+    import oracle  # noqa: F401
+    orc.store_kvcache(s["k"], s["v"], s["kc"].reshape(-1, W.HKV, W.HEAD_DIM), s["vc"].reshape(-1, W.HKV, W.HEAD_DIM),
+                      s["m"]["slot_mapping"])
+    orc.decode(s["q"], s["kc"], s["vc"], s["m"]["block_tables"], s["m"]["context_lens"], W.SCALE,
+               num_kv_heads=W.HKV)
+
+
+def cpu_baseline(c=None, budget_s=10.0, num_sample=16):
+    import oracle
+    orc = oracle.default()
+    s = _oracle_sample(num_sample)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        _oracle_step(orc, s)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": round(s["kv_bytes"] * reps / el / 1e9, 4), "unit": UNIT, "cores": orc.num_threads(),
+            "kind": "oracle", "sample": f"store + decode of the first {num_sample} of the 256 sequences "
+                                       f"(fp64 C oracle), repeated {reps}x over {el:.1f} s"}
+
+
+def run_reference(args):
+    import oracle
+    orc = oracle.default()
+    s = _oracle_sample(args.ref_sample)
+    for _ in range(args.warmup):
+        _oracle_step(orc, s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(orc, s)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    val = round(s["kv_bytes"] / (ms * 1e-3) / 1e9, 4)
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
+            "config": {"workload": "batched_decode_b256_ctx512-4096: store_kvcache(256 tokens) + GQA decode",
+                       "sample_seqs": args.ref_sample},
+            "cpu_baseline": {"value": val, "unit": UNIT, "kind": "oracle", "cores": orc.num_threads(),
+                             "sample": f"each step: store + decode of the first {args.ref_sample} of the 256 "
+                                       f"sequences with the fp64 C oracle"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-sample", type=int, default=8)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    try:
+        res = run_ours(args, rank, world, dev)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * The three operations are the attention block of a nano-vLLM style engine,
+ * as the pages walk through it:
+ *   - "vLLM 学习笔记 02：nano-vllm 源码逐段精读", layers/attention.py listing
+ *     (store_kvcache, then flash_attn_varlen_func for prefill or
+ *     flash_attn_with_kvcache for decode) and engine/model_runner.py listing
+ *     (how slot_mapping, cu_seqlens, block_tables and context_lens are built);
+ *   - "Nano-vLLM代码手撕笔记", sections "请求执行 – 输入序列预处理与context构建"
+ *     and "请求执行 – run model" (the same steps with a worked example).
+ *
+ * Conventions shared by every entry point
+ *   - Element type: bf16 for q, k, v, caches and outputs. Index arrays int32.
+ *   - Supported shape: head_dim = 128, block_size = 256; prefill and decode
+ *     also need num_kv_heads = 8 and num_heads = 16 (Qwen3-0.6B attention:
+ *     16 query heads grouped 2 per kv head). Query head h reads kv head
+ *     h / (num_heads / num_kv_heads).
+ *   - Cache layout: k_cache, v_cache are [num_blocks, 256, num_kv_heads, 128]
+ *     contiguous; token slot s is the row starting at element s*num_kv_heads*128.
+ *   - Pointers are DEVICE pointers owned by the caller unless stated. The
+ *     library allocates no memory, never synchronises a stream (except
+ *     pkv_device_error) and launches only on the stream it is given, so every
+ *     compute call can be captured in a CUDA graph.
+ *   - Return value: PKV_OK (0) or a negative PKV_ERR_* detected on the host
+ *     before anything is launched (then nothing is launched). Launch failures
+ *     return PKV_ERR_CUDA.
+ *   - Problems only visible on the device (a slot or block id outside the
+ *     pool, inconsistent cu_seqlens, a context longer than max_context_len)
+ *     never cause an out-of-bounds access: the offending work is skipped and a
+ *     bit is OR-ed into a per-device error word that pkv_device_error reads.
+ *     Outputs touched by skipped work are unspecified.
+ *   - Every device-side wait is bounded in time; a wait that runs out sets
+ *     PKV_DEVERR_TIMEOUT and the kernel returns instead of hanging.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side status codes. */
+#define PKV_OK 0
+#define PKV_ERR_NULL_POINTER (-1)      /* a required pointer is NULL */
+#define PKV_ERR_UNSUPPORTED (-2)       /* head_dim/block_size/head counts outside the supported shape */
+#define PKV_ERR_BAD_STRIDE (-3)        /* a row stride smaller than the row */
+#define PKV_ERR_ALIGNMENT (-4)         /* pointer or stride not 16-byte aligned where a kernel needs it */
+#define PKV_ERR_WORKSPACE (-5)         /* workspace NULL or smaller than the *_workspace_bytes query */
+#define PKV_ERR_BAD_SIZE (-6)          /* a negative count or a size beyond the library's limits */
+#define PKV_ERR_CUDA (-7)              /* a CUDA call or kernel launch failed */
+#define PKV_ERR_DEVICE (-8)            /* current device is not a compute capability 10.3 GPU */
+
+/* Device-side error bits (pkv_device_error). */
+#define PKV_DEVERR_BAD_SLOT 0x1u       /* slot_mapping entry not -1 and outside [0, num_slots) */
+#define PKV_DEVERR_BAD_BLOCK 0x2u      /* block_tables entry outside [0, num_blocks) where it is read */
+#define PKV_DEVERR_BAD_SEQLEN 0x4u     /* cu_seqlens not monotone, seqlen_k < seqlen_q, lengths above the
+                                          declared maxima, or a context longer than the block table */
+#define PKV_DEVERR_TIMEOUT 0x8u        /* a bounded device wait ran out */
+
+/* Human-readable text for a PKV_* status. Never NULL. */
+const char* pkv_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/*
+ * pkv_store_kvcache -- store_kvcache from layers/attention.py
+ * ("vLLM 学习笔记 02：nano-vllm 源码逐段精读"; explained in
+ * "Nano-vLLM代码手撕笔记", section "请求执行 – run model").
+ *
+ * For each token i < num_tokens with slot = slot_mapping[i] != -1:
+ *   k_cache[slot, :, :] = k[i, :, :]   and   v_cache[slot, :, :] = v[i, :, :]
+ * (num_kv_heads*head_dim elements each, a bit-exact copy). Tokens with
+ * slot -1 (padding) are skipped.
+ *
+ *   k, v            [num_tokens, num_kv_heads, head_dim] bf16; heads and
+ *                   dims contiguous within a row, rows k_row_stride /
+ *                   v_row_stride ELEMENTS apart (>= num_kv_heads*head_dim;
+ *                   e.g. 4096 for views of a fused qkv projection).
+ *   k_cache,v_cache [num_slots, num_kv_heads, head_dim] bf16, contiguous
+ *                   (num_slots = num_blocks * block_size).
+ *   slot_mapping    [num_tokens] int32.
+ * Any head_dim and num_kv_heads are accepted. When every pointer is 16-byte
+ * aligned and both row strides and the row length are multiples of 8
+ * elements, 16-byte vector copies are used; otherwise 2-byte copies.
+ * Duplicate slots in one call race (the pages never produce them); k/v must
+ * not overlap the caches. Slots outside [0, num_slots) set PKV_DEVERR_BAD_SLOT.
+ */
+int pkv_store_kvcache(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                      void* k_cache, void* v_cache, const int32_t* slot_mapping, int32_t num_tokens,
+                      int32_t num_kv_heads, int32_t head_dim, int64_t num_slots, cudaStream_t stream);
+
+/*
+ * pkv_prefill_varlen -- causal variable-length prefill attention, the
+ * flash_attn_varlen_func call of layers/attention.py with causal=True.
+ *
+ * Sequence b owns query rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q and
+ * Lk_b = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys. Query row i of sequence b
+ * sits at position Lk_b - Lq_b + i (prefix-cache hits and chunked prefill put
+ * the new tokens at the end, engine/model_runner.py prepare_prefill) and
+ * attends to keys 0..that position:
+ *   out[row, h, :] = softmax(softmax_scale * q[row, h, :] . K[0..p, h/G, :]^T) V[0..p, h/G, :]
+ * with fp32 logits and accumulation, bf16 output.
+ *
+ * Key source:
+ *   block_tables != NULL  (prefix-cache mode): key t of sequence b is slot
+ *     block_tables[b*block_table_stride + t/256]*256 + t%256 of k_cache/v_cache
+ *     ([num_blocks, 256, 8, 128]). The caller runs pkv_store_kvcache for the
+ *     new tokens first, on the same stream, as layers/attention.py does.
+ *     Entries past ceil(Lk_b/256) are never read.
+ *   block_tables == NULL  (no prefix hit): key t of sequence b is row
+ *     cu_seqlens_k[b] + t of k/v ([total_k, 8, 128], rows kv_row_stride
+ *     elements apart); k_cache/v_cache are ignored.
+ *
+ *   q    [total_q, 16, 128] bf16, rows q_row_stride elements apart.
+ *   out  [total_q, 16, 128] bf16 contiguous; every row of every sequence written.
+ *   total_q, total_k  row counts of q and of contiguous k/v (the tensors'
+ *        first dimension; total_k is ignored in prefix-cache mode). Tiles are
+ *        fetched by tensor-memory-access copies, which need the exact extent.
+ *   cu_seqlens_q/k [num_seqs+1] int32, max_seqlen_q/k their largest lengths;
+ *        cu_seqlens_q[num_seqs] <= total_q and, in contiguous mode,
+ *        cu_seqlens_k[num_seqs] <= total_k.
+ * q, k, v, k_cache, v_cache must be 16-byte aligned and their row strides
+ * multiples of 8 elements (tensor-memory-access rules). workspace may be
+ * NULL when pkv_prefill_workspace_bytes() is 0.
+ */
+int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                       int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                       int32_t num_blocks,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t max_seqlen_q,
+                       int32_t max_seqlen_k, const int32_t* block_tables, int32_t block_table_stride,
+                       int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, float softmax_scale, void* out, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes pkv_prefill_varlen needs for these sizes (may be 0). */
+size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
+
+/*
+ * pkv_decode -- single-query GQA decode attention over the paged cache, the
+ * flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache,
+ * cache_seqlens=context_lens, block_table=block_tables, causal=True) call of
+ * layers/attention.py.
+ *
+ * For sequence b and query head h, with ctx = context_lens[b] (the length
+ * including the token just stored, engine/model_runner.py prepare_decode):
+ *   out[b, h, :] = softmax(softmax_scale * q[b, h, :] . K_b[0..ctx-1]^T) V_b[0..ctx-1]
+ * where key t of sequence b is slot block_tables[b*block_table_stride + t/256]*256
+ * + t%256 of the kv head h/2. Rows with ctx == 0 (graph padding) get zeros.
+ * Entries of block_tables past ceil(ctx/256) are never read (they may be -1
+ * or stale).
+ *
+ *   q       [num_seqs, 16, 128] bf16, rows q_row_stride elements apart (>= 2048).
+ *   out     [num_seqs, 16, 128] bf16 contiguous.
+ *   max_context_len  upper bound on every context_lens[b] (e.g. max_model_len
+ *           when the call is captured in a graph and replayed with new lengths);
+ *           sizes the split-KV grid. Longer contexts set PKV_DEVERR_BAD_SEQLEN
+ *           and give zeros.
+ *   workspace  >= pkv_decode_workspace_bytes(num_seqs, num_heads, max_context_len)
+ *           bytes of device memory, ZERO-FILLED ONCE before its first use; every
+ *           call leaves it ready for the next. Calls that share a workspace
+ *           must not overlap in time (same stream, or ordered).
+ */
+int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+               int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+               const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+               int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
+               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes pkv_decode needs for these sizes. */
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len);
+
+/*
+ * pkv_device_error -- read (and optionally clear) the current device's
+ * error word (PKV_DEVERR_* bits OR-ed by every kernel of this library since
+ * the last clear). Synchronises `stream`, so do not call it inside a graph
+ * capture. bits may be NULL when only clearing.
+ */
+int pkv_device_error(uint32_t* bits, int clear, cudaStream_t stream);
+
+/*
+ * pkv_selftest_wait_timeout -- failure-detection self test: launches one
+ * block that waits on a barrier nothing will ever complete, with the given
+ * bound in nanoseconds (clamped to [1000, 100000000]). The wait must give
+ * up, set PKV_DEVERR_TIMEOUT and return; the GPU stays usable.
+ */
+int pkv_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,211 @@
+"""paged_kv_cache_kvh_gb300 -- Python binding of libpkv.so (attention over a paged KV cache, GB300).
+
+Argument marshalling only: every function here checks shapes, turns torch
+tensors into pointers, sizes and the current CUDA stream, and calls the C
+entry point of the same name (declared in ``include/pkv.h``). All work runs in
+the library's CUDA kernels; there is no CPU fallback. Importing this package
+fails loudly when ``libpkv.so`` has not been built
+(``python paged_kv_cache_kvh_gb300/build_lib.py``).
+
+Layouts (Qwen3-0.6B attention shape):
+  q            [tokens, 16, 128] bf16 (row stride may exceed 2048, e.g. fused qkv)
+  k, v         [tokens, 8, 128]  bf16
+  k/v caches   [num_blocks, 256, 8, 128] bf16 contiguous
+  slot_mapping, cu_seqlens_*, block_tables, context_lens  int32 on the GPU
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import metadata  # noqa: F401  (host index preparation)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK = 0
+PKV_DEVERR_BAD_SLOT = 0x1
+PKV_DEVERR_BAD_BLOCK = 0x2
+PKV_DEVERR_BAD_SEQLEN = 0x4
+PKV_DEVERR_TIMEOUT = 0x8
+HEAD_DIM, BLOCK_SIZE, NUM_HEADS, NUM_KV_HEADS = 128, 256, 16, 8
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libpkv.so is not built ({LIB_PATH}); run python paged_kv_cache_kvh_gb300/build_lib.py")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_i32, _i64, _u64, _vp, _f32, _sz = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p,
+                                     ctypes.c_float, ctypes.c_size_t)
+_SIGNATURES = {
+    "pkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pkv_version": (ctypes.c_int, []),
+    "pkv_store_kvcache": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp]),
+    "pkv_prefill_varlen": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _i32,
+                                          _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
+                                          _vp]),
+    "pkv_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pkv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                  _f32, _vp, _vp, _sz, _vp]),
+    "pkv_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pkv_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
+    "pkv_selftest_wait_timeout": (ctypes.c_int, [_u64, _vp]),
+}
+for _name, (_res, _args) in _SIGNATURES.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {pkv_status_string(status)} (status {status})")
+        self.status = status
+
+
+def pkv_status_string(status: int) -> str:
+    return _lib.pkv_status_string(int(status)).decode()
+
+
+def pkv_version() -> int:
+    return int(_lib.pkv_version())
+
+
+def _check(status: int, where: str):
+    if status != PKV_OK:
+        raise PkvError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _dev_i32(t, name):
+    _need(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous int32 CUDA tensor")
+
+
+def _rows(t, name, heads):
+    _need(t.dtype == torch.bfloat16 and t.is_cuda, f"{name} must be a bf16 CUDA tensor")
+    _need(t.dim() == 3 and t.shape[1] == heads and t.shape[2] == HEAD_DIM, f"{name} must be [N, {heads}, 128]")
+    _need(t.stride(2) == 1 and t.stride(1) == HEAD_DIM, f"{name}: heads and dims must be contiguous within a row")
+
+
+def pkv_store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """store_kvcache: k_cache[slot] = k[i], v_cache[slot] = v[i] for slot != -1."""
+    _need(k.dim() == 3 and v.shape == k.shape, "k, v must be [N, num_kv_heads, head_dim]")
+    N, hkv, d = k.shape
+    for t, n in ((k, "k"), (v, "v")):
+        _need(t.dtype == torch.bfloat16 and t.is_cuda and t.stride(2) == 1 and t.stride(1) == d,
+              f"{n}: bf16 CUDA, heads and dims contiguous")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape[-2:] == (hkv, d),
+              f"{n}: contiguous bf16 [..., {hkv}, {d}]")
+    _dev_i32(slot_mapping, "slot_mapping")
+    _need(slot_mapping.numel() == N, "slot_mapping must have one entry per token")
+    num_slots = k_cache.numel() // (hkv * d)
+    _check(_lib.pkv_store_kvcache(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(slot_mapping), N, hkv, d, num_slots, _stream(stream)), "pkv_store_kvcache")
+
+
+def pkv_prefill_workspace_bytes(num_seqs: int, max_seqlen_q: int, num_heads: int = NUM_HEADS) -> int:
+    return int(_lib.pkv_prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads))
+
+
+def pkv_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, *, k=None, v=None,
+                       k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None, stream=None):
+    """flash_attn_varlen_func(q, k, v, ..., causal=True, block_table=block_tables).
+
+    Paged keys (k_cache/v_cache through block_tables) when block_tables is
+    given, else contiguous k/v. Returns out [total_q, 16, 128] bf16."""
+    _rows(q, "q", NUM_HEADS)
+    _dev_i32(cu_seqlens_q, "cu_seqlens_q")
+    _dev_i32(cu_seqlens_k, "cu_seqlens_k")
+    num_seqs = cu_seqlens_q.numel() - 1
+    _need(cu_seqlens_k.numel() == num_seqs + 1, "cu_seqlens_k size")
+    total_q = q.shape[0]
+    if out is None:
+        out = torch.empty((total_q, NUM_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    _need(out.is_contiguous() and out.shape == (total_q, NUM_HEADS, HEAD_DIM) and out.dtype == torch.bfloat16,
+          "out must be contiguous bf16 [total_q, 16, 128]")
+    if block_tables is not None:
+        _dev_i32(block_tables, "block_tables")
+        for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+            _need(t is not None and t.dtype == torch.bfloat16 and t.is_contiguous()
+                  and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+        num_blocks, bt_stride = k_cache.shape[0], block_tables.shape[1]
+        kk = vv = None
+        kv_stride, total_k = 0, 0
+    else:
+        _rows(k, "k", NUM_KV_HEADS)
+        _rows(v, "v", NUM_KV_HEADS)
+        _need(k.stride(0) == v.stride(0) and k.shape == v.shape, "k and v must share shape and row stride")
+        kk, vv = k, v
+        kv_stride, total_k = k.stride(0), k.shape[0]
+        num_blocks, bt_stride = 0, 0
+    ws_bytes = pkv_prefill_workspace_bytes(num_seqs, int(max_seqlen_q))
+    _check(_lib.pkv_prefill_varlen(
+        _ptr(q), q.stride(0), total_q, _ptr(kk), _ptr(vv), kv_stride, total_k,
+        _ptr(k_cache) if block_tables is not None else None, _ptr(v_cache) if block_tables is not None else None,
+        num_blocks, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k),
+        _ptr(block_tables), bt_stride, num_seqs, NUM_HEADS, NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE,
+        float(softmax_scale), _ptr(out), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _stream(stream)), "pkv_prefill_varlen")
+    return out
+
+
+def pkv_decode_workspace_bytes(num_seqs: int, max_context_len: int, num_heads: int = NUM_HEADS) -> int:
+    return int(_lib.pkv_decode_workspace_bytes(num_seqs, num_heads, max_context_len))
+
+
+def decode_workspace(num_seqs: int, max_context_len: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for pkv_decode (allocated by torch, outside the library)."""
+    n = pkv_decode_workspace_bytes(num_seqs, max_context_len)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def pkv_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale, workspace, *,
+               out=None, stream=None):
+    """flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens=context_lens,
+    block_table=block_tables, causal=True). Returns out [num_seqs, 16, 128] bf16."""
+    _rows(q, "q", NUM_HEADS)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t.dtype == torch.bfloat16 and t.is_contiguous()
+              and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+    _dev_i32(block_tables, "block_tables")
+    _dev_i32(context_lens, "context_lens")
+    B = q.shape[0]
+    _need(block_tables.dim() == 2 and block_tables.shape[0] >= B and context_lens.numel() >= B, "table sizes")
+    if out is None:
+        out = torch.empty((B, NUM_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    _need(out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM), "out must be contiguous [B, 16, 128]")
+    _need(workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace must be a uint8 CUDA tensor")
+    _check(_lib.pkv_decode(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                           _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
+                           NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
+                           _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_decode")
+    return out
+
+
+def pkv_device_error(clear: bool = True, stream=None) -> int:
+    """Read (and by default clear) the device error word; synchronises the stream."""
+    bits = ctypes.c_uint32(0)
+    _check(_lib.pkv_device_error(ctypes.byref(bits), int(bool(clear)), _stream(stream)), "pkv_device_error")
+    return int(bits.value)
+
+
+def pkv_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None):
+    _check(_lib.pkv_selftest_wait_timeout(int(limit_ns), _stream(stream)), "pkv_selftest_wait_timeout")

@@ -1,0 +1,393 @@
+// decode.cu -- single-query GQA attention over the paged KV cache (split-KV).
+//
+// The operation is the flash_attn_with_kvcache call of layers/attention.py in
+// "vLLM 学习笔记 02：nano-vllm 源码逐段精读": one query per sequence, keys
+// 0..context_lens[b]-1 reached through block_tables, causal (a no-op for the
+// last position), query head h on kv head h/2.
+//
+// GB300 design (HBM-bound: 4 KB of K+V per token for 8 kv heads x 128 dims):
+//  * One CTA per (logical block c, sequence b): the block's tokens are one
+//    contiguous 512 KB K region and one 512 KB V region of the cache, so the
+//    producer warp streams them with plain bulk copies (cp.async.bulk, 1-D
+//    TMA), kT tokens x 2 KB per stage, through a kStages-deep shared-memory
+//    ring guarded by mbarriers.
+//  * Consumer warp w owns kv head w and both query heads 2w, 2w+1 that read
+//    it, so each K/V byte is loaded once for the whole GQA group. Lane l holds
+//    dims 4l..4l+3. Per stage every lane forms 2*kT partial dot products and a
+//    transposed butterfly (2*kT-1 shuffles for 2*kT results) leaves lane l
+//    with one complete logit; softmax statistics are half-warp reductions.
+//  * Split-KV merge without a second launch: each CTA writes (m, l, o) for its
+//    block to the workspace, and the CTA that finishes last for a sequence
+//    (atomic ticket, no waiting) merges them and resets the ticket to zero.
+//    Sequences with a single block write the output directly.
+//  * Logits are kept in the log2 domain (q is pre-scaled by scale*log2(e))
+//    and exponentials use ex2.approx.
+#include "pkv_common.cuh"
+
+#ifndef PKV_DECODE_TOKENS_PER_STAGE
+#define PKV_DECODE_TOKENS_PER_STAGE 16
+#endif
+#ifndef PKV_DECODE_STAGES
+#define PKV_DECODE_STAGES 3
+#endif
+
+namespace pkv {
+
+namespace {
+
+constexpr int kHkv = 8;
+constexpr int kGroup = 2;
+constexpr int kHq = kHkv * kGroup;
+constexpr int kRowBytes = kHkv * kHeadDim * 2;  // one token's K (or V) row: 2048 B
+constexpr int kConsumerWarps = kHkv;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  int64_t q_row_stride;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  int32_t num_blocks;
+  const int32_t* block_tables;
+  int32_t bt_stride;
+  const int32_t* context_lens;
+  int32_t max_ctx;
+  int32_t nsplit;
+  float scale_log2;
+  __nv_bfloat16* out;
+  int32_t* tickets;   // [num_seqs]
+  float2* ml;         // [num_seqs, nsplit, 16] (running max in log2 units, sum)
+  float* opart;       // [num_seqs, nsplit, 16, 128] unnormalised partial outputs
+  unsigned int* err;
+};
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+  return r;
+}
+
+// Transposed butterfly: lane l ends with the warp-wide sum of value index
+// (l >> (5 - log2 N)); N values per lane, N a power of two <= 32.
+template <int N>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
+  int n = N;
+  int offset = 16;
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    if (n > 1) {
+      const int half = n >> 1;
+      const bool upper = (lane & offset) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, offset);
+        }
+      }
+      n = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], offset);
+    }
+    offset >>= 1;
+  }
+  return v[0];
+}
+
+template <int kT, int kStages>
+__global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100 * 1024) ? 2 : 1)
+    decode_split_kernel(const DecodeParams p) {
+  static_assert(2 * kT <= 32 && (kT & (kT - 1)) == 0, "kT must be a power of two <= 16");
+  constexpr int kStageBytes = 2 * kT * kRowBytes;
+  constexpr int kN = 2 * kT;                 // logits per warp per stage
+  constexpr int kLog2N = (kN == 32) ? 5 : (kN == 16) ? 4 : (kN == 8) ? 3 : (kN == 4) ? 2 : 1;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* pbuf = reinterpret_cast<float*>(smem + kStages * kStageBytes);   // [8 warps][kN]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pbuf + kConsumerWarps * kN);
+  int* s_last = reinterpret_cast<int*>(bars + 2 * kStages);
+
+  const int c = blockIdx.x;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int ctx = p.context_lens[b];
+  if (ctx < 0 || ctx > p.max_ctx || ctx > p.bt_stride * kBlockSize) {
+    if (threadIdx.x == 0 && c == 0) flag_error(p.err, PKV_DEVERR_BAD_SEQLEN);
+    ctx = 0;
+  }
+  if (ctx == 0) {  // graph padding row: zeros
+    if (c == 0) {
+      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(b) * kHq * kHeadDim);
+      for (int i = threadIdx.x; i < kHq * kHeadDim / 8; i += blockDim.x) o[i] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const int nchunks = (ctx + kBlockSize - 1) / kBlockSize;
+  if (c >= nchunks) return;
+  const int ntok = min(kBlockSize, ctx - c * kBlockSize);
+  const int pb = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + c];
+  const bool bad_block = pb < 0 || pb >= p.num_blocks;
+  const int niter = bad_block ? 0 : (ntok + kT - 1) / kT;
+
+  const uint32_t smem0 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * kStages;
+  if (threadIdx.x == 0) {
+    if (bad_block) flag_error(p.err, PKV_DEVERR_BAD_BLOCK);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+  float m0 = -INFINITY, m1 = -INFINITY, lsum = 0.f;
+  const int h = warp;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer: one elected lane streams the block ----------------
+    if (lane == 0 && niter > 0) {
+      const int64_t base = static_cast<int64_t>(pb) * kBlockSize * kRowBytes;
+      const uint8_t* ksrc = p.k_cache + base;
+      const uint8_t* vsrc = p.v_cache + base;
+      int issued = 0;
+      for (int it = 0; it < niter; ++it) {
+        const int s = it % kStages;
+        if (it >= kStages && !mbar_wait(empty0 + 8 * s, ((it / kStages) - 1) & 1, p.err)) break;
+        const int rows = min(kT, ntok - it * kT);
+        const uint32_t bytes = static_cast<uint32_t>(rows) * kRowBytes;
+        const uint32_t dst = smem0 + s * kStageBytes;
+        mbar_arrive_expect_tx(full0 + 8 * s, 2 * bytes);
+        bulk_g2s(dst, ksrc + static_cast<int64_t>(it) * kT * kRowBytes, bytes, full0 + 8 * s);
+        bulk_g2s(dst + kT * kRowBytes, vsrc + static_cast<int64_t>(it) * kT * kRowBytes, bytes, full0 + 8 * s);
+        ++issued;
+      }
+      // Never leave a copy in flight into this CTA's shared memory.
+      for (int it = max(0, issued - kStages); it < issued; ++it)
+        mbar_wait(full0 + 8 * (it % kStages), (it / kStages) & 1, p.err);
+    }
+  } else {
+    // ---------------- consumers: warp h = kv head h, query heads 2h, 2h+1 ----------------
+    float q0[4], q1[4];
+    {
+      const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_row_stride;
+      const uint2 a = *reinterpret_cast<const uint2*>(qrow + (kGroup * h) * kHeadDim + lane * 4);
+      const uint2 bq = *reinterpret_cast<const uint2*>(qrow + (kGroup * h + 1) * kHeadDim + lane * 4);
+      q0[0] = bf16lo_to_f32(a.x) * p.scale_log2;
+      q0[1] = bf16hi_to_f32(a.x) * p.scale_log2;
+      q0[2] = bf16lo_to_f32(a.y) * p.scale_log2;
+      q0[3] = bf16hi_to_f32(a.y) * p.scale_log2;
+      q1[0] = bf16lo_to_f32(bq.x) * p.scale_log2;
+      q1[1] = bf16hi_to_f32(bq.x) * p.scale_log2;
+      q1[2] = bf16lo_to_f32(bq.y) * p.scale_log2;
+      q1[3] = bf16hi_to_f32(bq.y) * p.scale_log2;
+    }
+    const int idx = lane >> (5 - kLog2N);         // logit index this lane ends up holding
+    const int my_t = idx % kT;
+    const bool owner = (lane & ((1 << (5 - kLog2N)) - 1)) == 0;
+    const bool my_g1 = lane >= 16;
+    float* wp = pbuf + warp * kN;
+    const uint32_t wp_addr = smem_u32(wp);
+    for (int it = 0; it < niter; ++it) {
+      const int s = it % kStages;
+      // all lanes wait (each needs the acquire) and agree before the full-warp shuffles
+      if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (it / kStages) & 1, p.err))) break;
+      const int rows = min(kT, ntok - it * kT);
+      const uint32_t kaddr = smem0 + s * kStageBytes + h * (kHeadDim * 2) + lane * 8;
+      const uint32_t vaddr = kaddr + kT * kRowBytes;
+      float part[kN];
+#pragma unroll
+      for (int t = 0; t < kT; ++t) {
+        const uint2 kr = lds64(kaddr + t * kRowBytes);
+        const float k0 = bf16lo_to_f32(kr.x), k1 = bf16hi_to_f32(kr.x);
+        const float k2 = bf16lo_to_f32(kr.y), k3 = bf16hi_to_f32(kr.y);
+        part[t] = fmaf(q0[0], k0, fmaf(q0[1], k1, fmaf(q0[2], k2, q0[3] * k3)));
+        part[kT + t] = fmaf(q1[0], k0, fmaf(q1[1], k1, fmaf(q1[2], k2, q1[3] * k3)));
+      }
+      float sc = transpose_reduce<kN>(part, lane);
+      if (my_t >= rows) sc = -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mx0 = __shfl_sync(0xffffffffu, mx, 0);
+      const float mx1 = __shfl_sync(0xffffffffu, mx, 16);
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float mu1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float a0 = ex2_approx(m0 - mu0), a1 = ex2_approx(m1 - mu1);
+      const float pv = ex2_approx(sc - (my_g1 ? mu1 : mu0));
+      lsum = lsum * (my_g1 ? a1 : a0) + (owner ? pv : 0.f);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o0[i] *= a0;
+        o1[i] *= a1;
+      }
+      m0 = mn0;
+      m1 = mn1;
+      if (owner) wp[idx] = pv;
+      __syncwarp();
+#pragma unroll
+      for (int t = 0; t < kT; ++t) {
+        if (t < rows) {
+          float w0, w1;
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w0) : "r"(wp_addr + 4 * t));
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w1) : "r"(wp_addr + 4 * (kT + t)));
+          const uint2 vr = lds64(vaddr + t * kRowBytes);
+          const float v0 = bf16lo_to_f32(vr.x), v1 = bf16hi_to_f32(vr.x);
+          const float v2 = bf16lo_to_f32(vr.y), v3 = bf16hi_to_f32(vr.y);
+          o0[0] = fmaf(w0, v0, o0[0]);
+          o0[1] = fmaf(w0, v1, o0[1]);
+          o0[2] = fmaf(w0, v2, o0[2]);
+          o0[3] = fmaf(w0, v3, o0[3]);
+          o1[0] = fmaf(w1, v0, o1[0]);
+          o1[1] = fmaf(w1, v1, o1[1]);
+          o1[2] = fmaf(w1, v2, o1[2]);
+          o1[3] = fmaf(w1, v3, o1[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+    // row sums: half-warp g holds the partial sums of query head 2h+g
+    float l = lsum;
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    const float l0 = __shfl_sync(0xffffffffu, l, 0);
+    const float l1 = __shfl_sync(0xffffffffu, l, 16);
+    if (nchunks == 1) {
+      const float r0 = l0 > 0.f ? 1.f / l0 : 0.f, r1 = l1 > 0.f ? 1.f / l1 : 0.f;
+      __nv_bfloat16* orow = p.out + static_cast<int64_t>(b) * kHq * kHeadDim;
+      uint2 w;
+      w.x = pack_bf16x2(o0[0] * r0, o0[1] * r0);
+      w.y = pack_bf16x2(o0[2] * r0, o0[3] * r0);
+      *reinterpret_cast<uint2*>(orow + (kGroup * h) * kHeadDim + lane * 4) = w;
+      w.x = pack_bf16x2(o1[0] * r1, o1[1] * r1);
+      w.y = pack_bf16x2(o1[2] * r1, o1[3] * r1);
+      *reinterpret_cast<uint2*>(orow + (kGroup * h + 1) * kHeadDim + lane * 4) = w;
+    } else {
+      const int64_t slot = (static_cast<int64_t>(b) * p.nsplit + c) * kHq + kGroup * h;
+      *reinterpret_cast<float4*>(p.opart + slot * kHeadDim + lane * 4) = make_float4(o0[0], o0[1], o0[2], o0[3]);
+      *reinterpret_cast<float4*>(p.opart + (slot + 1) * kHeadDim + lane * 4) =
+          make_float4(o1[0], o1[1], o1[2], o1[3]);
+      if (lane == 0) {
+        p.ml[slot] = make_float2(m0, l0);
+        p.ml[slot + 1] = make_float2(m1, l1);
+      }
+    }
+  }
+
+  if (nchunks == 1) return;
+  // ---------------- split-KV merge by the last CTA of this sequence ----------------
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int prev = atomicAdd(p.tickets + b, 1);
+    *s_last = (prev == nchunks - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (*s_last == 0) return;
+  __threadfence();
+  if (threadIdx.x < kHq * 16) {
+    const int hq = threadIdx.x >> 4;
+    const int d0 = (threadIdx.x & 15) * 8;
+    const int64_t base = static_cast<int64_t>(b) * p.nsplit * kHq + hq;
+    float M = -INFINITY;
+    for (int cc = 0; cc < nchunks; ++cc) M = fmaxf(M, __ldcg(p.ml + base + static_cast<int64_t>(cc) * kHq).x);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float den = 0.f;
+    for (int cc = 0; cc < nchunks; ++cc) {
+      const int64_t slot = base + static_cast<int64_t>(cc) * kHq;
+      const float2 ml = __ldcg(p.ml + slot);
+      const float w = ex2_approx(ml.x - Mu);
+      den = fmaf(w, ml.y, den);
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(p.opart + slot * kHeadDim + d0));
+      const float4 y = __ldcg(reinterpret_cast<const float4*>(p.opart + slot * kHeadDim + d0 + 4));
+      acc[0] = fmaf(w, x.x, acc[0]);
+      acc[1] = fmaf(w, x.y, acc[1]);
+      acc[2] = fmaf(w, x.z, acc[2]);
+      acc[3] = fmaf(w, x.w, acc[3]);
+      acc[4] = fmaf(w, y.x, acc[4]);
+      acc[5] = fmaf(w, y.y, acc[5]);
+      acc[6] = fmaf(w, y.z, acc[6]);
+      acc[7] = fmaf(w, y.w, acc[7]);
+    }
+    const float r = den > 0.f ? 1.f / den : 0.f;
+    uint4 w;
+    w.x = pack_bf16x2(acc[0] * r, acc[1] * r);
+    w.y = pack_bf16x2(acc[2] * r, acc[3] * r);
+    w.z = pack_bf16x2(acc[4] * r, acc[5] * r);
+    w.w = pack_bf16x2(acc[6] * r, acc[7] * r);
+    *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + hq) * kHeadDim + d0) = w;
+  }
+  if (threadIdx.x == 0) p.tickets[b] = 0;  // ready for the next call
+}
+
+constexpr int kDecT = PKV_DECODE_TOKENS_PER_STAGE;
+constexpr int kDecStages = PKV_DECODE_STAGES;
+
+constexpr size_t decode_smem_bytes() {
+  return static_cast<size_t>(kDecStages) * 2 * kDecT * kRowBytes + kConsumerWarps * 2 * kDecT * sizeof(float) +
+         2 * kDecStages * sizeof(uint64_t) + 16;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+int decode_num_splits(int32_t max_context_len) { return (max_context_len + kBlockSize - 1) / kBlockSize; }
+
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len) {
+  const size_t ns = static_cast<size_t>(num_seqs);
+  const size_t nsplit = static_cast<size_t>(decode_num_splits(max_context_len));
+  return align_up(ns * sizeof(int32_t), 256) + align_up(ns * nsplit * kHq * sizeof(float2), 256) +
+         ns * nsplit * kHq * kHeadDim * sizeof(float);
+}
+
+cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                          int32_t num_blocks, const int32_t* block_tables, int32_t bt_stride,
+                          const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float scale,
+                          void* out, void* workspace, unsigned int* err, cudaStream_t stream) {
+  if (num_seqs == 0) return cudaSuccess;
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.q_row_stride = q_row_stride;
+  p.k_cache = static_cast<const uint8_t*>(k_cache);
+  p.v_cache = static_cast<const uint8_t*>(v_cache);
+  p.num_blocks = num_blocks;
+  p.block_tables = block_tables;
+  p.bt_stride = bt_stride;
+  p.context_lens = context_lens;
+  p.max_ctx = max_context_len;
+  p.nsplit = decode_num_splits(max_context_len);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t ns = static_cast<size_t>(num_seqs);
+  p.tickets = reinterpret_cast<int32_t*>(ws);
+  ws += align_up(ns * sizeof(int32_t), 256);
+  p.ml = reinterpret_cast<float2*>(ws);
+  ws += align_up(ns * p.nsplit * kHq * sizeof(float2), 256);
+  p.opart = reinterpret_cast<float*>(ws);
+  p.err = err;
+  if (p.nsplit == 0) p.nsplit = 1;
+  const size_t smem = decode_smem_bytes();
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kDecT, kDecStages>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const dim3 grid(p.nsplit, num_seqs);
+  decode_split_kernel<kDecT, kDecStages><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

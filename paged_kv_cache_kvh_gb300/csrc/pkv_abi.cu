@@ -1,0 +1,223 @@
+// pkv_abi.cu -- extern "C" entry points of libpkv.so (declared in include/pkv.h).
+//
+// Host-side argument checks mirror the asserts of store_kvcache in
+// layers/attention.py ("vLLM 学习笔记 02：nano-vllm 源码逐段精读": unit
+// element stride, heads contiguous, cache rows of num_kv_heads*head_dim,
+// one slot per token) plus the limits of these kernels; a failed check
+// returns an error code before anything is launched.
+#include <cstdio>
+
+#include "pkv_common.cuh"
+
+namespace pkv {
+cudaError_t launch_store_kvcache(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
+                                 void* k_cache, void* v_cache, const int32_t* slot_mapping, int32_t num_tokens,
+                                 int32_t D, int64_t num_slots, unsigned int* err, cudaStream_t stream);
+cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                          int32_t num_blocks, const int32_t* block_tables, int32_t bt_stride,
+                          const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float scale,
+                          void* out, void* workspace, unsigned int* err, cudaStream_t stream);
+size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len);
+cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                           int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                           int32_t num_blocks, const int32_t* cu_q, const int32_t* cu_k, int32_t max_seqlen_q,
+                           int32_t max_seqlen_k, const int32_t* block_tables, int32_t bt_stride, int32_t num_seqs,
+                           float scale, void* out, unsigned int* err, cudaStream_t stream);
+size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
+}  // namespace pkv
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Per-device error word: OR of PKV_DEVERR_* bits raised by any kernel.
+__device__ unsigned int g_pkv_error_word;
+
+unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+
+__global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* err) {
+  __shared__ __align__(8) uint64_t never;
+  const uint32_t bar = pkv::smem_u32(&never);
+  if (threadIdx.x == 0) {
+    pkv::mbar_init(bar, 1);  // one arrival expected, none will come
+    pkv::mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) pkv::mbar_wait(bar, 0, err, limit_ns);
+}
+
+// Address of this device's error word (looked up once per device).
+int error_word(unsigned int** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  if (!g_err_ptr[dev]) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return PKV_ERR_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pkv_error_word) != cudaSuccess) return PKV_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int launched(cudaError_t e) {
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+// The attention kernels are built for one head layout.
+int check_attention_shape(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size) {
+  if (head_dim != pkv::kHeadDim || block_size != pkv::kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (num_kv_heads != 8 || num_heads != 16) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape (head_dim 128, block_size 256, 16 q / 8 kv heads)";
+    case PKV_ERR_BAD_STRIDE: return "row stride smaller than the row";
+    case PKV_ERR_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_BAD_SIZE: return "negative count or size beyond the library's limits";
+    case PKV_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case PKV_ERR_DEVICE: return "current device is not compute capability 10.3";
+    default: return "unknown status";
+  }
+}
+
+int pkv_version(void) { return 100; }
+
+int pkv_store_kvcache(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride, void* k_cache,
+                      void* v_cache, const int32_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                      int32_t head_dim, int64_t num_slots, cudaStream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_slots < 0) return PKV_ERR_BAD_SIZE;
+  const int64_t D = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (D > (1 << 20)) return PKV_ERR_BAD_SIZE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_NULL_POINTER;
+  if (k_row_stride < D || v_row_stride < D) return PKV_ERR_BAD_STRIDE;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 1u)
+    return PKV_ERR_ALIGNMENT;
+  unsigned int* err = nullptr;
+  int st = error_word(&err);
+  if (st != PKV_OK) return st;
+  return launched(pkv::launch_store_kvcache(k, k_row_stride, v, v_row_stride, k_cache, v_cache, slot_mapping,
+                                            num_tokens, static_cast<int32_t>(D), num_slots, err, stream));
+}
+
+size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads) {
+  return pkv::prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads);
+}
+
+int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                       int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                       int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                       int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_tables,
+                       int32_t block_table_stride, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, float softmax_scale, void* out, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || num_blocks < 0 ||
+      block_table_stride < 0)
+    return PKV_ERR_BAD_SIZE;
+  if (num_seqs == 0 || total_q == 0 || max_seqlen_q == 0) return PKV_OK;
+  if (!(softmax_scale > 0.f)) return PKV_ERR_BAD_SIZE;
+  if (!q || !out || !cu_seqlens_q || !cu_seqlens_k) return PKV_ERR_NULL_POINTER;
+  const int64_t row = static_cast<int64_t>(num_heads) * head_dim;
+  const int64_t kvrow = static_cast<int64_t>(num_kv_heads) * head_dim;
+  if (q_row_stride < row) return PKV_ERR_BAD_STRIDE;
+  if (!aligned16(q) || (q_row_stride % 8) != 0 || !aligned16(out)) return PKV_ERR_ALIGNMENT;
+  if (block_tables) {
+    if (!k_cache || !v_cache) return PKV_ERR_NULL_POINTER;
+    if (num_blocks == 0 || block_table_stride == 0) return PKV_ERR_BAD_SIZE;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_ALIGNMENT;
+  } else {
+    if (!k || !v) return PKV_ERR_NULL_POINTER;
+    if (total_k == 0) return PKV_ERR_BAD_SIZE;
+    if (kv_row_stride < kvrow) return PKV_ERR_BAD_STRIDE;
+    if (!aligned16(k) || !aligned16(v) || (kv_row_stride % 8) != 0) return PKV_ERR_ALIGNMENT;
+  }
+  const size_t need = pkv::prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return PKV_ERR_WORKSPACE;
+  unsigned int* err = nullptr;
+  st = error_word(&err);
+  if (st != PKV_OK) return st;
+  return launched(pkv::launch_prefill(q, q_row_stride, total_q, k, v, kv_row_stride, total_k, k_cache, v_cache,
+                                      num_blocks, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                                      block_tables, block_table_stride, num_seqs, softmax_scale, out, err, stream));
+}
+
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len) {
+  (void)num_heads;
+  if (num_seqs <= 0 || max_context_len <= 0) return 0;
+  return pkv::decode_workspace_bytes(num_seqs, max_context_len);
+}
+
+int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
+               const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
+               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+  int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || num_blocks < 0 || block_table_stride < 0 || max_context_len < 0 ||
+      max_context_len > (1 << 24))
+    return PKV_ERR_BAD_SIZE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!(softmax_scale > 0.f)) return PKV_ERR_BAD_SIZE;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_NULL_POINTER;
+  if (q_row_stride < static_cast<int64_t>(num_heads) * head_dim) return PKV_ERR_BAD_STRIDE;
+  if (!aligned16(q) || (q_row_stride % 8) != 0 || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PKV_ERR_ALIGNMENT;
+  if (max_context_len > 0) {
+    const size_t need = pkv::decode_workspace_bytes(num_seqs, max_context_len);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGNMENT;
+  }
+  unsigned int* err = nullptr;
+  st = error_word(&err);
+  if (st != PKV_OK) return st;
+  return launched(pkv::launch_decode(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
+                                     block_table_stride, context_lens, num_seqs, max_context_len, softmax_scale,
+                                     out, workspace, err, stream));
+}
+
+int pkv_device_error(uint32_t* bits, int clear, cudaStream_t stream) {
+  unsigned int* err = nullptr;
+  int st = error_word(&err);
+  if (st != PKV_OK) return st;
+  unsigned int h = 0;
+  if (cudaMemcpyAsync(&h, err, sizeof(h), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return PKV_ERR_CUDA;
+  if (clear && cudaMemsetAsync(err, 0, sizeof(unsigned int), stream) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
+  if (bits) *bits = h;
+  return PKV_OK;
+}
+
+int pkv_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  unsigned int* err = nullptr;
+  int st = error_word(&err);
+  if (st != PKV_OK) return st;
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 100000000ull) limit_ns = 100000000ull;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return launched(cudaGetLastError());
+}
+
+}  // extern "C"

@@ -1,0 +1,178 @@
+"""Parity of store + decode (pkv_store_kvcache, pkv_decode) with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import HostPool, assert_close, bits, poison_dead_slots, pool_tensors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_kvh_gb300 as m
+    m.pkv_device_error(clear=True)
+    return m
+
+
+def _decode_step(pkv, wl, device, *, sample=None, poison=False, max_ctx=W.MAX_MODEL_LEN, fused=True,
+                 table_pad=0, stale_fill=None):
+    """Store the new token of every sequence, then decode; check against the oracle."""
+    gen = W.make_generator(wl.seed, device)
+    kc, vc = pool_tensors(wl.num_blocks, gen, device)
+    seqs = wl.seqs
+    B = len(seqs)
+    if fused:
+        _, q, k, v = W.fused_qkv(B, gen, device)
+    else:
+        q = W.normal_bf16((B, W.HQ, W.HEAD_DIM), gen, device)
+        k = W.normal_bf16((B, W.HKV, W.HEAD_DIM), gen, device)
+        v = W.normal_bf16((B, W.HKV, W.HEAD_DIM), gen, device)
+    if poison:
+        poison_dead_slots(kc, vc, seqs, lambda s: s.num_tokens)
+    width = max(len(s.block_table) for s in seqs) + table_pad
+    meta = pkv.metadata.prepare_decode(seqs, W.BLOCK_SIZE, table_width=width)
+    ometa = oracle.prepare_decode([oracle.SeqState(s.num_tokens, list(s.block_table)) for s in seqs], W.BLOCK_SIZE)
+    assert np.array_equal(meta["slot_mapping"], ometa["slot_mapping"])      # index work: bit-exact
+    assert np.array_equal(meta["context_lens"], ometa["context_lens"])
+    bt = meta["block_tables"]
+    if stale_fill is not None:  # entries past ceil(ctx/256) must never be read
+        for r, s in enumerate(seqs):
+            bt[r, len(s.block_table):] = stale_fill
+    sample = list(range(B)) if sample is None else sample
+    host = HostPool(kc, vc, [seqs[i] for i in sample])       # pre-store copy for the oracle
+    kb, vb, qb = bits(k), bits(v), bits(q)
+
+    slot = to_dev(meta["slot_mapping"], device)
+    ctx = to_dev(meta["context_lens"], device)
+    btd = to_dev(bt, device)
+    ws = pkv.decode_workspace(B, max_ctx, device)
+    pkv.pkv_store_kvcache(k, v, kc, vc, slot)
+    out = pkv.pkv_decode(q, kc, vc, btd, ctx, max_ctx, W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() == 0
+
+    # oracle: its own store into its own copy, then its own decode
+    om = oracle.prepare_decode(host.seqs, W.BLOCK_SIZE)
+    ks, vs = host.slots()
+    orc = oracle.default()
+    orc.store_kvcache(kb[sample], vb[sample], ks, vs, om["slot_mapping"])
+    ref = orc.decode(qb[sample], host.k, host.v, om["block_tables"], om["context_lens"], W.SCALE,
+                     num_kv_heads=W.HKV)
+    got = out[torch.tensor(sample, device=device)]
+    assert_close(got, ref, wl.name)
+    return out, (kc, vc, k, v, q, slot, ctx, btd, ws)
+
+
+def test_tiny_decode(pkv):
+    """4 sequences, context 37/256/300/511, 16-block pool (the whole case)."""
+    _decode_step(pkv, W.tiny_decode(), "cuda")
+
+
+def test_tiny_decode_poisoned_and_stale_tables(pkv):
+    """Dead slots hold NaN and table entries past ceil(ctx/256) are garbage:
+    neither may reach the output."""
+    _decode_step(pkv, W.tiny_decode(seed=11), "cuda", poison=True, table_pad=3, stale_fill=123456)
+
+
+@pytest.mark.parametrize("ctxs", [[1, 2, 255, 256, 257, 511, 512, 513, 1000, 4096],
+                                  [4096] * 3 + [1] * 3, [300]])
+def test_ragged_contexts(pkv, ctxs):
+    rng = np.random.default_rng(len(ctxs))
+    nb = sum(W.blocks_for(c) for c in ctxs) + 5
+    wl = W.Workload("ragged", 77, W._decode_seqs(ctxs, nb, rng), nb, "decode")
+    _decode_step(pkv, wl, "cuda", poison=True, fused=False)
+
+
+def test_batched_decode_full_size(pkv):
+    """256 sequences, context 512..4096, 8192-block pool: sampled sequences
+    (shortest, longest and a random spread) against the oracle."""
+    wl = W.batched_decode()
+    ctx = np.array([s.num_tokens for s in wl.seqs])
+    rng = np.random.default_rng(0)
+    sample = sorted({int(ctx.argmin()), int(ctx.argmax()), *rng.choice(len(ctx), 10, replace=False).tolist()})
+    _decode_step(pkv, wl, "cuda", sample=sample)
+
+
+def test_sweep_shape_one_layer(pkv):
+    """512 sequences with long-tailed contexts (1..4096): one layer, sampled."""
+    wl = W.sweep_decode(num_layers=1)
+    ctx = np.array([s.num_tokens for s in wl.seqs])
+    order = np.argsort(ctx)
+    sample = sorted({int(order[0]), int(order[1]), int(order[-1]), int(order[len(order) // 2]),
+                     *np.random.default_rng(1).choice(len(ctx), 8, replace=False).tolist()})
+    _decode_step(pkv, wl, "cuda", sample=sample)
+
+
+def test_padding_rows_and_repeat_calls(pkv):
+    """Graph-padding rows (slot -1, context 0) give zeros and write nothing;
+    a second call with the same workspace gives bit-identical output
+    (the split-KV tickets reset themselves)."""
+    dev = "cuda"
+    wl = W.tiny_decode(seed=5)
+    gen = W.make_generator(5, dev)
+    kc, vc = pool_tensors(wl.num_blocks, gen, dev)
+    meta = __import__("paged_kv_cache_kvh_gb300").metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE)
+    B, pad = len(wl.seqs), 4
+    q = W.normal_bf16((B + pad, W.HQ, W.HEAD_DIM), gen, dev)
+    k = W.normal_bf16((B + pad, W.HKV, W.HEAD_DIM), gen, dev)
+    v = W.normal_bf16((B + pad, W.HKV, W.HEAD_DIM), gen, dev)
+    slot = torch.full((B + pad,), -1, dtype=torch.int32, device=dev)
+    slot[:B] = to_dev(meta["slot_mapping"], dev)
+    ctx = torch.zeros(B + pad, dtype=torch.int32, device=dev)
+    ctx[:B] = to_dev(meta["context_lens"], dev)
+    bt = torch.zeros(B + pad, 16, dtype=torch.int32, device=dev)
+    bt[:B, :meta["block_tables"].shape[1]] = to_dev(meta["block_tables"], dev)
+    before_k = kc.clone()
+    ws = pkv.decode_workspace(B + pad, W.MAX_MODEL_LEN, dev)
+    pkv.pkv_store_kvcache(k, v, kc, vc, slot)
+    changed = (kc != before_k).flatten(1).any(dim=1).nonzero().flatten().tolist()
+    assert set(changed) <= {int(s) // (W.BLOCK_SIZE) for s in meta["slot_mapping"]}
+    o1 = pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+    o2 = pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+    assert torch.all(o1[B:] == 0)
+    assert pkv.pkv_device_error() == 0
+
+
+def test_context_beyond_declared_max_is_flagged(pkv):
+    dev = "cuda"
+    wl = W.tiny_decode(seed=6)
+    gen = W.make_generator(6, dev)
+    kc, vc = pool_tensors(wl.num_blocks, gen, dev)
+    meta = __import__("paged_kv_cache_kvh_gb300").metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE)
+    q = W.normal_bf16((4, W.HQ, W.HEAD_DIM), gen, dev)
+    ws = pkv.decode_workspace(4, 256, dev)
+    out = pkv.pkv_decode(q, kc, vc, to_dev(meta["block_tables"], dev), to_dev(meta["context_lens"], dev), 256,
+                         W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_SEQLEN
+    assert torch.all(out[2:] == 0)          # contexts 300 and 511 exceed 256: zeros
+    assert torch.all(torch.isfinite(out[:2].float()))
+
+
+def test_bad_block_and_slot_are_flagged_not_dereferenced(pkv):
+    dev = "cuda"
+    gen = W.make_generator(9, dev)
+    kc, vc = pool_tensors(4, gen, dev)
+    q = W.normal_bf16((2, W.HQ, W.HEAD_DIM), gen, dev)
+    k = W.normal_bf16((2, W.HKV, W.HEAD_DIM), gen, dev)
+    bt = torch.tensor([[0, 1 << 20], [-5, 0]], dtype=torch.int32, device=dev)
+    ctx = torch.tensor([300, 10], dtype=torch.int32, device=dev)
+    ws = pkv.decode_workspace(2, 512, dev)
+    pkv.pkv_decode(q, kc, vc, bt, ctx, 512, W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_BLOCK
+    pkv.pkv_store_kvcache(k, k, kc, vc, torch.tensor([5, 4 * 256], dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_SLOT
+    # the device is still healthy
+    out = pkv.pkv_decode(q, kc, vc, torch.tensor([[0, 1], [2, 3]], dtype=torch.int32, device=dev), ctx, 512,
+                         W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert torch.all(torch.isfinite(out.float())) and pkv.pkv_device_error() == 0

@@ -1,0 +1,164 @@
+"""Parity of store + varlen prefill (pkv_store_kvcache, pkv_prefill_varlen) with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import HostPool, assert_close, bits, poison_dead_slots, pool_tensors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_kv_cache_kvh_gb300 as m
+    m.pkv_device_error(clear=True)
+    return m
+
+
+def _seqs_with_tables(specs, rng, spare=3):
+    """specs: list of (num_cached, num_scheduled). Blocks from a shuffled pool."""
+    need = sum(W.blocks_for(c + s) for c, s in specs)
+    nb = need + spare
+    perm = rng.permutation(nb)
+    cur, seqs = 0, []
+    for c, s in specs:
+        n = c + s
+        t = [int(x) for x in perm[cur:cur + W.blocks_for(n)]]
+        cur += len(t)
+        seqs.append(W.SeqSpec(num_tokens=n, block_table=t, num_cached_tokens=c, num_scheduled_tokens=s))
+    return seqs, nb
+
+
+def _rows_sample(cu_q, rng, per_seq=6):
+    rows = []
+    for b in range(len(cu_q) - 1):
+        lq = int(cu_q[b + 1] - cu_q[b])
+        if lq == 0:
+            continue
+        picks = {0, lq - 1, *rng.integers(0, lq, size=min(per_seq, lq)).tolist()}
+        for i in picks:
+            rows.append((int(cu_q[b]) + i, int(rng.integers(0, W.HQ))))
+    return np.array(rows, dtype=np.int64)
+
+
+def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguous=False):
+    """Store the scheduled tokens of every sequence, run paged prefill, compare
+    with the oracle (all rows, or sampled rows) and optionally with the
+    contiguous-keys mode of the same kernel."""
+    dev = "cuda"
+    gen = W.make_generator(seed, dev)
+    kc, vc = pool_tensors(nb, gen, dev)
+    T = sum(s.num_scheduled_tokens for s in seqs)
+    _, q, k, v = W.fused_qkv(T, gen, dev)
+    if poison:
+        poison_dead_slots(kc, vc, seqs, lambda s: s.num_tokens)
+    meta = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
+    ometa = oracle.prepare_prefill([oracle.SeqState(s.num_tokens, list(s.block_table), s.num_cached_tokens,
+                                                    s.num_scheduled_tokens) for s in seqs], W.BLOCK_SIZE)
+    for key in ("slot_mapping", "cu_seqlens_q", "cu_seqlens_k", "positions"):
+        assert np.array_equal(meta[key], ometa[key]), key
+    host = HostPool(kc, vc, seqs)
+    qb, kb, vb = bits(q), bits(k), bits(v)
+
+    slot = to_dev(meta["slot_mapping"], dev)
+    cu_q = to_dev(meta["cu_seqlens_q"], dev)
+    cu_k = to_dev(meta["cu_seqlens_k"], dev)
+    bt = to_dev(meta["block_tables"], dev)
+    pkv.pkv_store_kvcache(k, v, kc, vc, slot)
+    out = pkv.pkv_prefill_varlen(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE,
+                                 k_cache=kc, v_cache=vc, block_tables=bt)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() == 0
+
+    om = oracle.prepare_prefill(host.seqs, W.BLOCK_SIZE)
+    ks, vs = host.slots()
+    orc = oracle.default()
+    orc.store_kvcache(kb, vb, ks, vs, om["slot_mapping"])
+    bt_o = oracle.pad_block_tables(host.seqs)
+    ref = orc.prefill_varlen(qb, om["cu_seqlens_q"], om["cu_seqlens_k"], W.SCALE, k_cache=host.k, v_cache=host.v,
+                             block_tables=bt_o, num_kv_heads=W.HKV, rows=sample_rows)
+    if sample_rows is None:
+        assert_close(out, ref, "prefill")
+    else:
+        got = out[torch.from_numpy(sample_rows[:, 0]).to(dev), torch.from_numpy(sample_rows[:, 1]).to(dev)]
+        assert_close(got, ref, "prefill (sampled rows)")
+    if check_contiguous:
+        # no prefix: the same keys from contiguous k/v must give the identical result
+        out2 = pkv.pkv_prefill_varlen(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k=k, v=v)
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2)
+    return out
+
+
+@pytest.mark.parametrize("lens", [[1], [5, 2], [127, 128, 129], [1, 255, 256, 257, 300, 513], [1024, 77]])
+def test_prefill_no_prefix(pkv, lens):
+    rng = np.random.default_rng(sum(lens))
+    seqs, nb = _seqs_with_tables([(0, n) for n in lens], rng)
+    _run(pkv, seqs, nb, seed=len(lens), poison=True, check_contiguous=True)
+
+
+@pytest.mark.parametrize("specs", [
+    [(256, 10)],                       # prefix of one whole block
+    [(1024, 64), (1024, 512)],         # prefix of 4 blocks
+    [(1, 1), (300, 129), (44, 300)],   # chunked prefill starting mid-block
+    [(511, 1), (257, 255), (128, 128)],
+    [(3000, 1000)],                    # long context
+])
+def test_prefill_with_cached_prefix(pkv, specs):
+    rng = np.random.default_rng(len(specs) + sum(c for c, _ in specs))
+    seqs, nb = _seqs_with_tables(specs, rng)
+    _run(pkv, seqs, nb, seed=sum(s for _, s in specs), poison=True)
+
+
+def test_varlen_prefill_full_size(pkv):
+    """64 prompts of 100..1024 tokens in <=16384-token calls, paged, sampled rows."""
+    wl = W.varlen_prefill()
+    rng = np.random.default_rng(3)
+    for i, call in enumerate(wl.seqs):
+        cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in call])])
+        _run(pkv, call, wl.num_blocks, seed=100 + i, sample_rows=_rows_sample(cu, rng, 4), check_contiguous=True)
+
+
+def test_prefix_prefill_full_size(pkv):
+    """128 sequences sharing a 1024-token prefix in 4 blocks, suffixes 64..512, sampled rows."""
+    wl = W.prefix_prefill()
+    call = wl.seqs[0]
+    cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in call])])
+    _run(pkv, call, wl.num_blocks, seed=4, sample_rows=_rows_sample(cu, np.random.default_rng(4), 3))
+
+
+def test_identical_sequences_identical_outputs(pkv):
+    """Two sequences sharing the same prefix blocks, with identical suffix
+    tokens, produce bit-identical outputs (prefix-cache reuse is exact)."""
+    dev = "cuda"
+    gen = W.make_generator(21, dev)
+    kc, vc = pool_tensors(8, gen, dev)
+    s = 200
+    _, q1, k1, v1 = W.fused_qkv(s, gen, dev)
+    q = torch.cat([q1, q1]).contiguous()
+    k = torch.cat([k1, k1]).contiguous()
+    v = torch.cat([v1, v1]).contiguous()
+    seqs = [W.SeqSpec(1024 + s, [0, 1, 2, 3, 4], 1024, s), W.SeqSpec(1024 + s, [0, 1, 2, 3, 5], 1024, s)]
+    meta = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE)
+    pkv.pkv_store_kvcache(k, v, kc, vc, to_dev(meta["slot_mapping"], dev))
+    out = pkv.pkv_prefill_varlen(q, to_dev(meta["cu_seqlens_q"], dev), to_dev(meta["cu_seqlens_k"], dev),
+                                 meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc,
+                                 block_tables=to_dev(meta["block_tables"], dev))
+    torch.cuda.synchronize()
+    assert torch.equal(out[:s], out[s:])
+
+
+def test_bad_seqlens_flagged(pkv):
+    dev = "cuda"
+    gen = W.make_generator(22, dev)
+    q = W.normal_bf16((10, W.HQ, W.HEAD_DIM), gen, dev)
+    k = W.normal_bf16((10, W.HKV, W.HEAD_DIM), gen, dev)
+    cu_q = torch.tensor([0, 6, 10], dtype=torch.int32, device=dev)
+    cu_k = torch.tensor([0, 4, 10], dtype=torch.int32, device=dev)   # first sequence: Lk < Lq
+    pkv.pkv_prefill_varlen(q, cu_q, cu_k, 6, 6, W.SCALE, k=k, v=k)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_SEQLEN
