@@ -54,6 +54,7 @@ extern "C" {
 #define PKV_ERR_BAD_SIZE (-6)          /* a negative count or a size beyond the library's limits */
 #define PKV_ERR_CUDA (-7)              /* a CUDA call or kernel launch failed */
 #define PKV_ERR_DEVICE (-8)            /* current device is not a compute capability 10.3 GPU */
+#define PKV_ERR_SCRATCH_LIMIT (-9)     /* pkv_decode_noalloc: the sizes need more than its built-in scratch */
 
 /* Device-side error bits (pkv_device_error). */
 #define PKV_DEVERR_BAD_SLOT 0x1u       /* slot_mapping entry not -1 and outside [0, num_slots) */
@@ -174,6 +175,42 @@ int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const v
 
 /* Workspace bytes pkv_decode needs for these sizes. */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len);
+
+/*
+ * pkv_decode_noalloc -- pkv_decode for callers that cannot allocate device
+ * memory. The pages have no counterpart to this entry point: it exists for
+ * users of this library, not for the method.
+ *
+ * Who needs it: an engine that sized its KV-cache pool to take all device
+ * memory left after start-up (nano-vLLM does exactly this), a plug-in whose
+ * host process owns the only device allocator, or a latency-critical loop
+ * that must not call cudaMalloc because it can synchronise the device. None
+ * of them can hand pkv_decode a workspace.
+ *
+ * Same arguments and result as pkv_decode, without the workspace: the
+ * split-KV scratch lives in a fixed array of PKV_DECODE_NOALLOC_SCRATCH_BYTES
+ * that is part of the library's device image, reserved on every GPU that
+ * loads the library and held until the process exits. The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - Limit: sizes with pkv_decode_workspace_bytes(num_seqs, num_heads,
+ *     max_context_len) > PKV_DECODE_NOALLOC_SCRATCH_BYTES are rejected with
+ *     PKV_ERR_SCRATCH_LIMIT before anything is launched (e.g. 256 sequences
+ *     with max_context_len 4096 fit; 512 sequences fit up to 2048).
+ *   - The first call on each device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress) and caches it; make that
+ *     first call before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; each
+ *     call first clears (cudaMemsetAsync on `stream`) the part that must start
+ *     at zero. Calls whose execution overlaps on the GPU (different streams
+ *     without ordering, or several host threads) race on the array and give
+ *     wrong results: order them.
+ */
+#define PKV_DECODE_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int pkv_decode_noalloc(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                       int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale,
+                       void* out, cudaStream_t stream);
 
 /*
  * pkv_device_error -- read (and optionally clear) the current device's

@@ -30,6 +30,8 @@ PKV_DEVERR_BAD_SLOT = 0x1
 PKV_DEVERR_BAD_BLOCK = 0x2
 PKV_DEVERR_BAD_SEQLEN = 0x4
 PKV_DEVERR_TIMEOUT = 0x8
+PKV_ERR_SCRATCH_LIMIT = -9
+PKV_DECODE_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 HEAD_DIM, BLOCK_SIZE, NUM_HEADS, NUM_KV_HEADS = 128, 256, 16, 8
 
 if not os.path.exists(LIB_PATH):
@@ -49,6 +51,8 @@ _SIGNATURES = {
     "pkv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _vp, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pkv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                          _i32, _f32, _vp, _vp]),
     "pkv_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
     "pkv_selftest_wait_timeout": (ctypes.c_int, [_u64, _vp]),
 }
@@ -197,6 +201,32 @@ def pkv_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len,
                            _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
                            NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
                            _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_decode")
+    return out
+
+
+def pkv_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale, out, *,
+                       stream=None):
+    """pkv_decode without a workspace, for callers that cannot allocate device
+    memory (a KV pool that already took all free memory, a host that owns the
+    only allocator, a loop that must not synchronise on cudaMalloc). Scratch
+    comes from a fixed array inside the library, so the caller passes the
+    output buffer too and nothing is allocated. Sizes beyond that array
+    (PKV_DECODE_NOALLOC_SCRATCH_BYTES) raise PkvError(PKV_ERR_SCRATCH_LIMIT).
+    Calls must not overlap on the GPU: they share the array."""
+    _rows(q, "q", NUM_HEADS)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t.dtype == torch.bfloat16 and t.is_contiguous()
+              and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+    _dev_i32(block_tables, "block_tables")
+    _dev_i32(context_lens, "context_lens")
+    B = q.shape[0]
+    _need(block_tables.dim() == 2 and block_tables.shape[0] >= B and context_lens.numel() >= B, "table sizes")
+    _need(out is not None and out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM)
+          and out.dtype == torch.bfloat16, "out must be a caller-owned contiguous bf16 [B, 16, 128]")
+    _check(_lib.pkv_decode_noalloc(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                   _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
+                                   NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
+                                   _ptr(out), _stream(stream)), "pkv_decode_noalloc")
     return out
 
 

@@ -1,0 +1,74 @@
+// decode_noalloc.cu -- pkv_decode_noalloc: decode attention for callers that
+// cannot allocate device memory.
+//
+// pkv_decode needs a caller-provided workspace for its split-KV partial
+// results. Some callers have no way to provide one: an engine that sized its
+// KV-cache pool to take all device memory left after start-up, a plug-in whose
+// host process owns the only device allocator, or a latency-critical loop
+// that must not call cudaMalloc (it can synchronise the device). For them this
+// entry point runs the same decode with its scratch in a fixed array that is
+// part of the library's device image: it is reserved on every GPU that loads
+// the library and held until the process exits, so nothing is allocated per
+// call.
+//
+// The array has no device address known to host code until it is looked up:
+// in host code its name only stands for a host-side shadow symbol, and handing
+// that to a kernel would fault or, where the GPU can reach host memory,
+// silently touch the wrong memory. So the first call on each device (with that
+// device current) asks the runtime for the real address with
+// cudaGetSymbolAddress, checks the result, caches it per device, and every
+// call passes that address on to the kernel.
+#include "pkv_common.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// The scratch itself: PKV_DECODE_NOALLOC_SCRATCH_BYTES bytes per device.
+static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[PKV_DECODE_NOALLOC_SCRATCH_BYTES];
+
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of this device's scratch array (looked up once per device).
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_decode_noalloc(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                                  int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                                  const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t max_context_len, float softmax_scale, void* out, cudaStream_t stream) {
+  if (num_seqs < 0 || max_context_len < 0) return PKV_ERR_BAD_SIZE;
+  if (num_seqs == 0) return PKV_OK;
+  const size_t need = pkv_decode_workspace_bytes(num_seqs, num_heads, max_context_len);
+  if (need > static_cast<size_t>(PKV_DECODE_NOALLOC_SCRATCH_BYTES)) return PKV_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  int st = scratch_address(&scratch);
+  if (st != PKV_OK) return st;
+  // The split-KV tickets at the start of the scratch must start at zero. The
+  // array keeps whatever the previous call left, so clear them on the stream.
+  if (need > 0) {
+    const size_t tickets = static_cast<size_t>(num_seqs) * sizeof(int32_t);
+    if (cudaMemsetAsync(scratch, 0, tickets, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+  }
+  return pkv_decode(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride, context_lens,
+                    num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len, softmax_scale, out,
+                    scratch, static_cast<size_t>(PKV_DECODE_NOALLOC_SCRATCH_BYTES), stream);
+}

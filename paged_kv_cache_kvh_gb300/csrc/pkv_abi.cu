@@ -95,6 +95,7 @@ const char* pkv_status_string(int status) {
     case PKV_ERR_BAD_SIZE: return "negative count or size beyond the library's limits";
     case PKV_ERR_CUDA: return "CUDA call or kernel launch failed";
     case PKV_ERR_DEVICE: return "current device is not compute capability 10.3";
+    case PKV_ERR_SCRATCH_LIMIT: return "sizes need more scratch than pkv_decode_noalloc's built-in array";
     default: return "unknown status";
   }
 }
