@@ -124,6 +124,20 @@ def _flush_l2(buf):
     buf.zero_()
 
 
+def max_over_ranks(ms, world, device):
+    """Slowest rank's time: every rank does the same work (replicas)."""
+    if world <= 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, ms_step):
+    """Whole-job units per second: all ranks' units over the slowest rank's step time."""
+    return world * units_per_rank / (ms_step * 1e-3)
+
+
 # ---------------------------------------------------------------------------
 # the decode step (ours)
 # ---------------------------------------------------------------------------
@@ -181,12 +195,8 @@ def run_ours(args, rank, world, dev):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
-    ms_total = t0.elapsed_time(t1)
     dec_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms_total / args.steps
     err = pkv.pkv_device_error()
     if err:
@@ -201,7 +211,7 @@ def run_ours(args, rank, world, dev):
             "unit": "GB/s", "frac": round(ach / hbm, 4), "peak_source": f"{src} (hbm copy)",
             "alg_bytes_per_launch": c["decode_alg_bytes"], "avg_launch_ms": round(dec_ms, 5),
             "traffic": _traffic("decode.cu", c["kv_bytes"])}
-    res = {"metric": METRIC, "value": round(world * c["kv_bytes"] / (ms_step * 1e-3) / 1e9, 1), "unit": UNIT,
+    res = {"metric": METRIC, "value": round(job_throughput(c["kv_bytes"], world, ms_step) / 1e9, 1), "unit": UNIT,
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
            "data": "synthetic (seeded N(0,1) bf16, shuffled block tables)",
@@ -215,6 +225,8 @@ def run_ours(args, rank, world, dev):
            "roofline": roof, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
     if rank == 0 and not args.no_prefill:
         res["prefill"] = run_prefill(pkv, args, dev, bf16)
+    if rank == 0 and not args.no_sweep:
+        res["sweep"] = run_sweep(pkv, args, dev, hbm)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(c, budget_s=args.cpu_seconds)
     return res
@@ -315,6 +327,111 @@ def run_prefill(pkv, args, dev, bf16_peak):
     return res
 
 
+def run_sweep(pkv, args, dev, hbm_peak):
+    """28 layers x (store 512 tokens + decode 512 sequences), one CUDA graph."""
+    wl = W.sweep_decode()
+    L, B = wl.num_layers, len(wl.seqs)
+    gen = W.make_generator(wl.seed, dev)
+    kv = W.normal_bf16((2, L, wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM), gen, dev)
+    qkv = [W.fused_qkv(B, gen, dev) for _ in range(L)]
+    meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE, table_width=W.MAX_MODEL_LEN // W.BLOCK_SIZE)
+    slot = torch.from_numpy(meta["slot_mapping"]).to(dev)
+    ctx = torch.from_numpy(meta["context_lens"]).to(dev)
+    bt = torch.from_numpy(meta["block_tables"]).to(dev)
+    ws = pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev)
+    outs = torch.empty(L, B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+
+    def sweep():
+        for l in range(L):
+            _, q, k, v = qkv[l]
+            pkv.pkv_store_kvcache(k, v, kv[0, l], kv[1, l], slot)
+            pkv.pkv_decode(q, kv[0, l], kv[1, l], bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws, out=outs[l])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        sweep()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sweep()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(args.steps, 20))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    kv_bytes = L * int(meta["context_lens"].astype(np.int64).sum()) * W.HKV * W.HEAD_DIM * 4
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    assert pkv.pkv_device_error() == 0
+    del kv, g
+    torch.cuda.empty_cache()
+    return {"workload": "decode_sweep_28l_b512_ctx_geometric800: 28 x (store 512 tokens + decode), one CUDA graph",
+            "num_blocks": wl.num_blocks, "cache_gb": round(2 * L * wl.num_blocks * 256 * 8 * 128 * 2 / 1e9, 1),
+            "sum_context_lens": int(meta["context_lens"].sum()), "ms_per_sweep": round(ms, 4),
+            "kv_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4), "replays": reps,
+            "gpu_launches_per_sweep": 2 * L}
+
+
+def ncu_case(kind):
+    """Small single-kernel cases for ncu captures (a few launches, a few GB)."""
+    import paged_kv_cache_kvh_gb300 as pkv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if kind == "decode":
+        wl = W.batched_decode()
+        seqs = wl.seqs[:64]
+        used = sorted({b for s in seqs for b in s.block_table})
+        remap = {b: i for i, b in enumerate(used)}
+        seqs = [W.SeqSpec(s.num_tokens, [remap[b] for b in s.block_table]) for s in seqs]
+        gen = W.make_generator(2, dev)
+        shape = (len(used), W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+        kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
+        _, q, k, v = W.fused_qkv(len(seqs), gen, dev)
+        m = pkv.metadata.prepare_decode(seqs, W.BLOCK_SIZE, table_width=16)
+        ws = pkv.decode_workspace(len(seqs), W.MAX_MODEL_LEN, dev)
+        bt, ctx = torch.from_numpy(m["block_tables"]).to(dev), torch.from_numpy(m["context_lens"]).to(dev)
+        for _ in range(3):
+            pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+        units = int(m["context_lens"].astype(np.int64).sum()) * W.HKV * W.HEAD_DIM * 4
+    elif kind in ("prefill", "prefill_prefix"):
+        wl = W.varlen_prefill() if kind == "prefill" else W.prefix_prefill()
+        seqs = wl.seqs[0]
+        gen = W.make_generator(wl.seed, dev)
+        shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+        kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
+        T = sum(s.num_scheduled_tokens for s in seqs)
+        _, q, k, v = W.fused_qkv(T, gen, dev)
+        m = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
+        d = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
+        pkv.pkv_store_kvcache(k, v, kc, vc, d(m["slot_mapping"]))
+        for _ in range(3):
+            pkv.pkv_prefill_varlen(q, d(m["cu_seqlens_q"]), d(m["cu_seqlens_k"]), m["max_seqlen_q"],
+                                   m["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc, block_tables=d(m["block_tables"]))
+        units = _prefill_flops(seqs)
+    elif kind == "store":
+        gen = W.make_generator(3, dev)
+        N = 16384
+        kc = W.normal_bf16((160, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM), gen, dev)
+        vc = W.normal_bf16((160, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM), gen, dev)
+        _, q, k, v = W.fused_qkv(N, gen, dev)
+        slot = torch.from_numpy(np.random.default_rng(3).permutation(160 * 256)[:N].astype(np.int32)).to(dev)
+        for _ in range(3):
+            pkv.pkv_store_kvcache(k, v, kc, vc, slot)
+        units = N * W.HKV * W.HEAD_DIM * 8
+    else:
+        raise SystemExit(f"unknown ncu case {kind}")
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() == 0
+    print(json.dumps({"ncu_case": kind, "units": units}))
+
+
 # ---------------------------------------------------------------------------
 # oracle (CPU) arm
 # ---------------------------------------------------------------------------
@@ -396,8 +513,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-sample", type=int, default=8)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "store"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.ncu_case:
+        ncu_case(args.ncu_case)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
