@@ -25,7 +25,7 @@
 #include "pkv_common.cuh"
 
 #ifndef PKV_DECODE_TOKENS_PER_STAGE
-#define PKV_DECODE_TOKENS_PER_STAGE 16
+#define PKV_DECODE_TOKENS_PER_STAGE 8
 #endif
 #ifndef PKV_DECODE_STAGES
 #define PKV_DECODE_STAGES 3
