@@ -173,6 +173,29 @@ int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const v
                int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * pkv_store_decode -- store_kvcache fused into the decode step
+ * (layers/attention.py runs store_kvcache, then flash_attn_with_kvcache, on
+ * the same slot_mapping; "vLLM 学习笔记 02：nano-vllm 源码逐段精读").
+ *
+ * Same result as pkv_store_kvcache(k, k_row_stride, v, v_row_stride, k_cache,
+ * v_cache, slot_mapping, num_seqs, ...) followed by pkv_decode(...), in one
+ * launch: the CTA that streams sequence b's last block first writes the new
+ * K/V row there. It requires what engine/model_runner.py prepare_decode
+ * produces: slot_mapping[b] is -1 (padding, nothing stored) or the slot of
+ * position context_lens[b]-1 of sequence b. Any other slot is not stored and
+ * sets PKV_DEVERR_BAD_SLOT.
+ *   k, v  [num_seqs, 8, 128] bf16, rows k_row_stride / v_row_stride elements
+ *         apart, 16-byte aligned, strides multiples of 8 elements.
+ * Every other argument is as for pkv_decode.
+ */
+int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                     int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                     int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                     const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Workspace bytes pkv_decode needs for these sizes. */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len);
 

@@ -51,6 +51,8 @@ _SIGNATURES = {
     "pkv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _vp, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pkv_store_decode": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32,
+                                        _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "pkv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _vp, _vp]),
     "pkv_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
@@ -227,6 +229,34 @@ def pkv_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_cont
                                    _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
                                    NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
                                    _ptr(out), _stream(stream)), "pkv_decode_noalloc")
+    return out
+
+
+def pkv_store_decode(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                     softmax_scale, workspace, *, out=None, stream=None):
+    """store_kvcache of the step's new K/V rows fused into the decode launch.
+    slot_mapping[b] must be -1 or the slot of position context_lens[b]-1."""
+    _rows(q, "q", NUM_HEADS)
+    _rows(k, "k", NUM_KV_HEADS)
+    _rows(v, "v", NUM_KV_HEADS)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t.dtype == torch.bfloat16 and t.is_contiguous()
+              and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+    _dev_i32(slot_mapping, "slot_mapping")
+    _dev_i32(block_tables, "block_tables")
+    _dev_i32(context_lens, "context_lens")
+    B = q.shape[0]
+    _need(k.shape[0] >= B and v.shape[0] >= B and slot_mapping.numel() >= B, "one new row per sequence")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] >= B and context_lens.numel() >= B, "table sizes")
+    if out is None:
+        out = torch.empty((B, NUM_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+    _need(out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM), "out must be contiguous [B, 16, 128]")
+    _need(workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace must be a uint8 CUDA tensor")
+    _check(_lib.pkv_store_decode(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(v), v.stride(0),
+                                 _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                 _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
+                                 NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
+                                 _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_store_decode")
     return out
 
 

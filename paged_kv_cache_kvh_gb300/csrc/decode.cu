@@ -33,6 +33,15 @@
 
 namespace pkv {
 
+// New-token rows for pkv_store_decode (k/v row strides in elements).
+struct FusedStore {
+  const void* k;
+  int64_t k_row_stride;
+  const void* v;
+  int64_t v_row_stride;
+  const int32_t* slot_mapping;
+};
+
 namespace {
 
 constexpr int kHkv = 8;
@@ -58,6 +67,14 @@ struct DecodeParams {
   int32_t* tickets;   // [num_seqs]
   float2* ml;         // [num_seqs, nsplit, 16] (running max in log2 units, sum)
   float* opart;       // [num_seqs, nsplit, 16, 128] unnormalised partial outputs
+  // Fused store (pkv_store_decode); k_new == nullptr for plain decode.
+  const uint4* k_new;
+  const uint4* v_new;
+  int64_t k_new_stride16;  // row strides in 16-byte units
+  int64_t v_new_stride16;
+  const int32_t* slot_mapping;
+  uint4* k_cache_w;
+  uint4* v_cache_w;
   unsigned int* err;
 };
 
@@ -134,6 +151,25 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
   const uint32_t smem0 = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * kStages;
+  if (p.k_new != nullptr && c == nchunks - 1) {
+    // Fused store: this CTA owns the sequence's newest position ctx-1, whose
+    // slot the new token's K/V row must reach before the block is streamed.
+    const int64_t slot = p.slot_mapping[b];
+    if (slot != -1) {
+      const int64_t expect = static_cast<int64_t>(pb) * kBlockSize + (ctx - 1) % kBlockSize;
+      if (bad_block || slot != expect) {
+        if (threadIdx.x == 0) flag_error(p.err, PKV_DEVERR_BAD_SLOT);
+      } else if (threadIdx.x < 2 * kRowBytes / 16) {
+        const bool is_v = threadIdx.x >= kRowBytes / 16;
+        const int i = threadIdx.x % (kRowBytes / 16);
+        const uint4* src = is_v ? p.v_new + b * p.v_new_stride16 : p.k_new + b * p.k_new_stride16;
+        uint4* dst = (is_v ? p.v_cache_w : p.k_cache_w) + slot * (kRowBytes / 16);
+        dst[i] = src[i];
+        // make the write visible to the bulk copies (async proxy) issued after the CTA barrier
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+    }
+  }
   if (threadIdx.x == 0) {
     if (bad_block) flag_error(p.err, PKV_DEVERR_BAD_BLOCK);
     for (int s = 0; s < kStages; ++s) {
@@ -351,9 +387,17 @@ size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len) {
 cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
                           int32_t num_blocks, const int32_t* block_tables, int32_t bt_stride,
                           const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float scale,
-                          void* out, void* workspace, unsigned int* err, cudaStream_t stream) {
+                          void* out, void* workspace, unsigned int* err, cudaStream_t stream,
+                          const FusedStore* fused) {
   if (num_seqs == 0) return cudaSuccess;
   DecodeParams p;
+  p.k_new = fused ? static_cast<const uint4*>(fused->k) : nullptr;
+  p.v_new = fused ? static_cast<const uint4*>(fused->v) : nullptr;
+  p.k_new_stride16 = fused ? fused->k_row_stride / 8 : 0;
+  p.v_new_stride16 = fused ? fused->v_row_stride / 8 : 0;
+  p.slot_mapping = fused ? fused->slot_mapping : nullptr;
+  p.k_cache_w = static_cast<uint4*>(const_cast<void*>(k_cache));
+  p.v_cache_w = static_cast<uint4*>(const_cast<void*>(v_cache));
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.q_row_stride = q_row_stride;
   p.k_cache = static_cast<const uint8_t*>(k_cache);

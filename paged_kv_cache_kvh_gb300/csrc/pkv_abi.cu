@@ -13,10 +13,18 @@ namespace pkv {
 cudaError_t launch_store_kvcache(const void* k, int64_t k_row_stride, const void* v, int64_t v_row_stride,
                                  void* k_cache, void* v_cache, const int32_t* slot_mapping, int32_t num_tokens,
                                  int32_t D, int64_t num_slots, unsigned int* err, cudaStream_t stream);
+struct FusedStore {
+  const void* k;
+  int64_t k_row_stride;
+  const void* v;
+  int64_t v_row_stride;
+  const int32_t* slot_mapping;
+};
 cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
                           int32_t num_blocks, const int32_t* block_tables, int32_t bt_stride,
                           const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float scale,
-                          void* out, void* workspace, unsigned int* err, cudaStream_t stream);
+                          void* out, void* workspace, unsigned int* err, cudaStream_t stream,
+                          const FusedStore* fused = nullptr);
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len);
 cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
                            int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
@@ -170,11 +178,14 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t m
   return pkv::decode_workspace_bytes(num_seqs, max_context_len);
 }
 
-int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
-               const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
-               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-               int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
-               cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+int decode_common(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                  const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
+                  int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                  int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream, const pkv::FusedStore* fused) {
   int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || num_blocks < 0 || block_table_stride < 0 || max_context_len < 0 ||
@@ -196,7 +207,39 @@ int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const v
   if (st != PKV_OK) return st;
   return launched(pkv::launch_decode(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
                                      block_table_stride, context_lens, num_seqs, max_context_len, softmax_scale,
-                                     out, workspace, err, stream));
+                                     out, workspace, err, stream, fused));
+}
+}  // namespace
+
+extern "C" {
+
+int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
+               const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
+               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+  return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                       softmax_scale, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                     int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                     int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                     const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (num_seqs > 0) {
+    if (!k || !v || !slot_mapping) return PKV_ERR_NULL_POINTER;
+    const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
+    if (k_row_stride < row || v_row_stride < row) return PKV_ERR_BAD_STRIDE;
+    if (!aligned16(k) || !aligned16(v) || (k_row_stride % 8) != 0 || (v_row_stride % 8) != 0)
+      return PKV_ERR_ALIGNMENT;
+  }
+  const pkv::FusedStore fused{k, k_row_stride, v, v_row_stride, slot_mapping};
+  return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                       softmax_scale, out, workspace, workspace_bytes, stream, &fused);
 }
 
 int pkv_device_error(uint32_t* bits, int clear, cudaStream_t stream) {

@@ -328,6 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + 64, r2);
         tmem_ld32(tS + 96, r3);
         tmem_wait_ld();
+        tmem_reg_fence(r0);
+        tmem_reg_fence(r1);
+        tmem_reg_fence(r2);
+        tmem_reg_fence(r3);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           s[j] = __uint_as_float(r0[j]);
@@ -373,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t r[32];
           tmem_ld32(tO + c * 32, r);
           tmem_wait_ld();
+          tmem_reg_fence(r);
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
           tmem_st32(tO + c * 32, r);
@@ -396,6 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
         tmem_ld32(tO + c * 32, r);
         tmem_wait_ld();
+        tmem_reg_fence(r);
         if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {

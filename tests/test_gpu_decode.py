@@ -176,3 +176,51 @@ def test_bad_block_and_slot_are_flagged_not_dereferenced(pkv):
                          W.SCALE, ws)
     torch.cuda.synchronize()
     assert torch.all(torch.isfinite(out.float())) and pkv.pkv_device_error() == 0
+
+
+@pytest.mark.parametrize("factory", [W.tiny_decode, W.batched_decode, lambda: W.sweep_decode(num_layers=1)])
+def test_store_decode_fused_matches_separate(pkv, factory):
+    """pkv_store_decode == pkv_store_kvcache then pkv_decode: same output and
+    the same cache, bit for bit (padding rows included)."""
+    dev = "cuda"
+    wl = factory()
+    gen = W.make_generator(wl.seed + 1000, dev)
+    kc, vc = pool_tensors(wl.num_blocks, gen, dev)
+    B, pad = len(wl.seqs), 3
+    _, q, k, v = W.fused_qkv(B + pad, gen, dev)
+    meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE, table_width=16)
+    slot = torch.full((B + pad,), -1, dtype=torch.int32, device=dev)
+    slot[:B] = to_dev(meta["slot_mapping"], dev)
+    ctx = torch.zeros(B + pad, dtype=torch.int32, device=dev)
+    ctx[:B] = to_dev(meta["context_lens"], dev)
+    bt = torch.zeros(B + pad, 16, dtype=torch.int32, device=dev)
+    bt[:B] = to_dev(meta["block_tables"], dev)
+    kc2, vc2 = kc.clone(), vc.clone()
+    ws = pkv.decode_workspace(B + pad, W.MAX_MODEL_LEN, dev)
+    pkv.pkv_store_kvcache(k, v, kc, vc, slot)
+    ref = pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+    got = pkv.pkv_store_decode(q, k, v, slot, kc2, vc2, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() == 0
+    assert torch.equal(got, ref)
+    assert torch.equal(kc2, kc) and torch.equal(vc2, vc)
+
+
+def test_store_decode_rejects_foreign_slot(pkv):
+    """A slot that is not the sequence's newest position is flagged, not stored."""
+    dev = "cuda"
+    wl = W.tiny_decode(seed=8)
+    gen = W.make_generator(8, dev)
+    kc, vc = pool_tensors(wl.num_blocks, gen, dev)
+    _, q, k, v = W.fused_qkv(4, gen, dev)
+    meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE)
+    slot = to_dev(meta["slot_mapping"], dev)
+    slot[1] = slot[1] - 1                         # one position too early
+    before = kc.clone()
+    ws = pkv.decode_workspace(4, W.MAX_MODEL_LEN, dev)
+    pkv.pkv_store_decode(q, k, v, slot, kc, vc, to_dev(meta["block_tables"], dev),
+                         to_dev(meta["context_lens"], dev), W.MAX_MODEL_LEN, W.SCALE, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_SLOT
+    bad = int(meta["slot_mapping"][1]) - 1
+    assert torch.equal(kc.view(-1, 8, 128)[bad], before.view(-1, 8, 128)[bad])

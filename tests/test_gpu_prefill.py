@@ -162,3 +162,13 @@ def test_bad_seqlens_flagged(pkv):
     pkv.pkv_prefill_varlen(q, cu_q, cu_k, 6, 6, W.SCALE, k=k, v=k)
     torch.cuda.synchronize()
     assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_SEQLEN
+
+
+def test_many_items_per_cta_with_tail_tiles(pkv):
+    """Hundreds of short sequences: every CTA of the persistent kernel takes
+    many work items in a row, most ending in a partial (zeroed) V tile."""
+    rng = np.random.default_rng(99)
+    specs = [(int(c), int(s)) for c, s in zip(rng.integers(0, 300, 400), rng.integers(1, 200, 400))]
+    seqs, nb = _seqs_with_tables(specs, rng)
+    cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in seqs])])
+    _run(pkv, seqs, nb, seed=99, poison=True, sample_rows=_rows_sample(cu, np.random.default_rng(5), 3))
