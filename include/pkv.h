@@ -236,6 +236,39 @@ int pkv_decode_noalloc(const void* q, int64_t q_row_stride, const void* k_cache,
                        void* out, cudaStream_t stream);
 
 /*
+ * pkv_build_prefill_metadata / pkv_build_decode_metadata -- the per-step index
+ * preparation of engine/model_runner.py (prepare_prefill, prepare_decode in
+ * "vLLM 学习笔记 02：nano-vllm 源码逐段精读"; worked example in
+ * "Nano-vLLM代码手撕笔记", section "请求执行 – 输入序列预处理与context构建"),
+ * computed on the GPU from what the scheduler has per sequence, so no
+ * per-token host loop and no per-token host-to-device copy is needed.
+ * Bit-identical to the host definition. A token whose block-table entry is
+ * outside [0, num_blocks) gets slot -1 and sets PKV_DEVERR_BAD_BLOCK.
+ *
+ * Prefill: sequence b computes positions [num_cached_tokens[b],
+ * num_cached_tokens[b] + num_scheduled_tokens[b]).
+ *   cu_seqlens_q[num_seqs+1]  prefix sums of num_scheduled_tokens
+ *   cu_seqlens_k[num_seqs+1]  prefix sums of num_cached + num_scheduled
+ *   max_seqlens[2]            {max_seqlen_q, max_seqlen_k} (device; the
+ *                             attention calls accept any upper bounds instead)
+ *   slot_mapping[capacity], positions[capacity] (int64)  one entry per new
+ *                             token, sequence by sequence; tokens beyond
+ *                             `capacity` are not written (PKV_DEVERR_BAD_SEQLEN).
+ * Decode: num_tokens[b] = len(seq) including the token being stored;
+ *   slot_mapping[b] = slot of position len-1, context_lens[b] = len,
+ *   positions[b] = len-1; rows with len 0 are padding (slot -1, context 0).
+ * All arrays are int32 device arrays except positions (int64, as the pages'
+ * torch.int64 positions). block_tables is [num_seqs, block_table_stride], -1 padded.
+ */
+int pkv_build_prefill_metadata(const int32_t* num_cached_tokens, const int32_t* num_scheduled_tokens,
+                               const int32_t* block_tables, int32_t block_table_stride, int32_t num_blocks,
+                               int32_t num_seqs, int32_t capacity, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
+                               int32_t* max_seqlens, int32_t* slot_mapping, int64_t* positions, cudaStream_t stream);
+int pkv_build_decode_metadata(const int32_t* num_tokens, const int32_t* block_tables, int32_t block_table_stride,
+                              int32_t num_blocks, int32_t num_seqs, int32_t* slot_mapping, int32_t* context_lens,
+                              int64_t* positions, cudaStream_t stream);
+
+/*
  * pkv_device_error -- read (and optionally clear) the current device's
  * error word (PKV_DEVERR_* bits OR-ed by every kernel of this library since
  * the last clear). Synchronises `stream`, so do not call it inside a graph

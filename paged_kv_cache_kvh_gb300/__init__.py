@@ -56,6 +56,9 @@ _SIGNATURES = {
     "pkv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _vp, _vp]),
     "pkv_device_error": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int, _vp]),
+    "pkv_build_prefill_metadata": (ctypes.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+                                                  _vp]),
+    "pkv_build_decode_metadata": (ctypes.c_int, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
     "pkv_selftest_wait_timeout": (ctypes.c_int, [_u64, _vp]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
@@ -257,6 +260,45 @@ def pkv_store_decode(q, k, v, slot_mapping, k_cache, v_cache, block_tables, cont
                                  _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
                                  NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
                                  _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_store_decode")
+    return out
+
+
+def pkv_build_prefill_metadata(num_cached_tokens, num_scheduled_tokens, block_tables, num_blocks, capacity,
+                               stream=None):
+    """prepare_prefill on the GPU. Inputs int32 CUDA tensors ([B], [B], [B, W]).
+    Returns dict of device tensors: cu_seqlens_q, cu_seqlens_k, max_seqlens (2),
+    slot_mapping [capacity], positions [capacity] (int64)."""
+    for t, n in ((num_cached_tokens, "num_cached_tokens"), (num_scheduled_tokens, "num_scheduled_tokens"),
+                 (block_tables, "block_tables")):
+        _dev_i32(t, n)
+    B = num_cached_tokens.numel()
+    _need(num_scheduled_tokens.numel() == B and block_tables.dim() == 2 and block_tables.shape[0] == B, "sizes")
+    dev = num_cached_tokens.device
+    out = dict(cu_seqlens_q=torch.empty(B + 1, dtype=torch.int32, device=dev),
+               cu_seqlens_k=torch.empty(B + 1, dtype=torch.int32, device=dev),
+               max_seqlens=torch.empty(2, dtype=torch.int32, device=dev),
+               slot_mapping=torch.empty(max(capacity, 1), dtype=torch.int32, device=dev),
+               positions=torch.empty(max(capacity, 1), dtype=torch.int64, device=dev))
+    _check(_lib.pkv_build_prefill_metadata(
+        _ptr(num_cached_tokens), _ptr(num_scheduled_tokens), _ptr(block_tables), block_tables.shape[1], int(num_blocks),
+        B, int(capacity), _ptr(out["cu_seqlens_q"]), _ptr(out["cu_seqlens_k"]), _ptr(out["max_seqlens"]),
+        _ptr(out["slot_mapping"]), _ptr(out["positions"]), _stream(stream)), "pkv_build_prefill_metadata")
+    return out
+
+
+def pkv_build_decode_metadata(num_tokens, block_tables, num_blocks, stream=None):
+    """prepare_decode on the GPU: slot_mapping, context_lens, positions (int64)."""
+    _dev_i32(num_tokens, "num_tokens")
+    _dev_i32(block_tables, "block_tables")
+    B = num_tokens.numel()
+    _need(block_tables.dim() == 2 and block_tables.shape[0] >= B, "block_tables [B, W]")
+    dev = num_tokens.device
+    out = dict(slot_mapping=torch.empty(B, dtype=torch.int32, device=dev),
+               context_lens=torch.empty(B, dtype=torch.int32, device=dev),
+               positions=torch.empty(B, dtype=torch.int64, device=dev))
+    _check(_lib.pkv_build_decode_metadata(_ptr(num_tokens), _ptr(block_tables), block_tables.shape[1],
+                                          int(num_blocks), B, _ptr(out["slot_mapping"]), _ptr(out["context_lens"]),
+                                          _ptr(out["positions"]), _stream(stream)), "pkv_build_decode_metadata")
     return out
 
 

@@ -32,6 +32,14 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
                            int32_t max_seqlen_k, const int32_t* block_tables, int32_t bt_stride, int32_t num_seqs,
                            float scale, void* out, unsigned int* err, cudaStream_t stream);
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
+cudaError_t launch_prefill_metadata(const int32_t* num_cached, const int32_t* num_scheduled,
+                                    const int32_t* block_tables, int32_t bt_stride, int32_t num_blocks,
+                                    int32_t num_seqs, int32_t capacity, int32_t* cu_q, int32_t* cu_k,
+                                    int32_t* max_q_k, int32_t* slot_mapping, int64_t* positions, unsigned int* err,
+                                    cudaStream_t stream);
+cudaError_t launch_decode_metadata(const int32_t* num_tokens, const int32_t* block_tables, int32_t bt_stride,
+                                   int32_t num_blocks, int32_t num_seqs, int32_t* slot_mapping, int32_t* context_lens,
+                                   int64_t* positions, unsigned int* err, cudaStream_t stream);
 }  // namespace pkv
 
 namespace {
@@ -240,6 +248,36 @@ int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t
   return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
                        context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
                        softmax_scale, out, workspace, workspace_bytes, stream, &fused);
+}
+
+int pkv_build_prefill_metadata(const int32_t* num_cached_tokens, const int32_t* num_scheduled_tokens,
+                               const int32_t* block_tables, int32_t block_table_stride, int32_t num_blocks,
+                               int32_t num_seqs, int32_t capacity, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
+                               int32_t* max_seqlens, int32_t* slot_mapping, int64_t* positions, cudaStream_t stream) {
+  if (num_seqs < 0 || num_seqs > 65535 || capacity < 0 || block_table_stride < 0 || num_blocks < 0)
+    return PKV_ERR_BAD_SIZE;
+  if (!cu_seqlens_q || !cu_seqlens_k || !max_seqlens) return PKV_ERR_NULL_POINTER;
+  if (num_seqs > 0 && (!num_cached_tokens || !num_scheduled_tokens || !block_tables || !slot_mapping || !positions))
+    return PKV_ERR_NULL_POINTER;
+  unsigned int* err = nullptr;
+  int st = error_word(&err);
+  if (st != PKV_OK) return st;
+  return launched(pkv::launch_prefill_metadata(num_cached_tokens, num_scheduled_tokens, block_tables,
+                                               block_table_stride, num_blocks, num_seqs, capacity, cu_seqlens_q,
+                                               cu_seqlens_k, max_seqlens, slot_mapping, positions, err, stream));
+}
+
+int pkv_build_decode_metadata(const int32_t* num_tokens, const int32_t* block_tables, int32_t block_table_stride,
+                              int32_t num_blocks, int32_t num_seqs, int32_t* slot_mapping, int32_t* context_lens,
+                              int64_t* positions, cudaStream_t stream) {
+  if (num_seqs < 0 || block_table_stride < 0 || num_blocks < 0) return PKV_ERR_BAD_SIZE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!num_tokens || !block_tables || !slot_mapping || !context_lens || !positions) return PKV_ERR_NULL_POINTER;
+  unsigned int* err = nullptr;
+  int st = error_word(&err);
+  if (st != PKV_OK) return st;
+  return launched(pkv::launch_decode_metadata(num_tokens, block_tables, block_table_stride, num_blocks, num_seqs,
+                                              slot_mapping, context_lens, positions, err, stream));
 }
 
 int pkv_device_error(uint32_t* bits, int clear, cudaStream_t stream) {
