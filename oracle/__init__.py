@@ -45,8 +45,19 @@ ORACLE_ERRORS = {
 }
 
 
+# Element types of q, k, v and the caches (the store copies bits and has none).
+ELEM_CODES = {"bf16": 0, "f16": 1}
+
+
 class OracleError(RuntimeError):
     pass
+
+
+def _elem(dtype: str) -> int:
+    try:
+        return ELEM_CODES[dtype]
+    except KeyError:
+        raise OracleError(f"unknown element type {dtype!r}") from None
 
 
 def build(src: str = _SRC, out: str = _LIB_PATH, force: bool = False) -> str:
@@ -76,11 +87,14 @@ class Oracle:
         L.oracle_store_kvcache.restype = ctypes.c_int
         L.oracle_store_kvcache.argtypes = [vp, i64, vp, i64, vp, vp, vp, i64, i64, i64]
         L.oracle_prefill_varlen.restype = ctypes.c_int
+        ci = ctypes.c_int
         L.oracle_prefill_varlen.argtypes = [vp, i64, vp, vp, i64, vp, vp, i64, vp, vp, vp, i64,
-                                            i64, i64, i64, i64, i64, dbl, vp, i64, vp]
+                                            i64, i64, i64, i64, i64, dbl, vp, i64, ci, vp]
         L.oracle_decode.restype = ctypes.c_int
         L.oracle_decode.argtypes = [vp, vp, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, dbl,
-                                    vp, i64, vp]
+                                    vp, i64, ci, vp]
+        L.oracle_elements_to_double.restype = ctypes.c_int
+        L.oracle_elements_to_double.argtypes = [vp, i64, ci, vp]
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
@@ -90,8 +104,16 @@ class Oracle:
         if status != 0:
             raise OracleError(ORACLE_ERRORS.get(status, f"status {status}"))
 
+    def elements_to_f64(self, bits, dtype: str = "bf16") -> np.ndarray:
+        """Widen 16-bit patterns of element type ``dtype`` to float64, exactly."""
+        b = np.ascontiguousarray(bits, dtype=np.uint16)
+        out = np.empty(b.shape, dtype=np.float64)
+        self._check(self.lib.oracle_elements_to_double(_ptr(b), b.size, _elem(dtype), _ptr(out)))
+        return out
+
     def store_kvcache(self, k, v, k_cache, v_cache, slot_mapping):
-        """In place on ``k_cache``/``v_cache`` (uint16 bf16 bits, [slots, Hkv, d]).
+        """In place on ``k_cache``/``v_cache`` (uint16 bit patterns of any 16-bit
+        element type, [slots, Hkv, d]).
 
         ``k``/``v`` are [N, Hkv, d] uint16 arrays whose last two axes are
         contiguous; their first-axis stride may exceed Hkv*d (views into a
@@ -110,10 +132,12 @@ class Oracle:
             _ptr(slot), N, D, num_slots))
 
     def prefill_varlen(self, q, cu_seqlens_q, cu_seqlens_k, scale, *, k_cache=None, v_cache=None,
-                       block_tables=None, k=None, v=None, num_kv_heads, block_size=256, rows=None):
+                       block_tables=None, k=None, v=None, num_kv_heads, block_size=256, rows=None,
+                       dtype="bf16"):
         """Causal varlen prefill. Paged when ``block_tables`` is given, else
         contiguous ``k``/``v``. Returns float64 [total_q, Hq, d], or [n, d]
-        for ``rows`` = int64 array of (token, head) pairs."""
+        for ``rows`` = int64 array of (token, head) pairs. ``dtype`` ("bf16"
+        or "f16") is the element type of the uint16 bit patterns passed in."""
         total_q, Hq, d = q.shape
         assert q.dtype == np.uint16 and q.strides[2] == 2 and q.strides[1] == 2 * d
         cu_q = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
@@ -145,12 +169,13 @@ class Oracle:
         self._check(self.lib.oracle_prefill_varlen(
             _ptr(q), q.strides[0] // 2, _ptr(kk), _ptr(vv), kv_stride, _ptr(kc), _ptr(vc), num_blocks,
             _ptr(cu_q), _ptr(cu_k), _ptr(bt), bt_stride, num_seqs, Hq, num_kv_heads, d, block_size,
-            float(scale), _ptr(rows_arr), n_rows, _ptr(out)))
+            float(scale), _ptr(rows_arr), n_rows, _elem(dtype), _ptr(out)))
         return out
 
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale, *, num_kv_heads,
-               block_size=256, seqs=None):
-        """Single-query paged decode. Returns float64 [B or len(seqs), Hq, d]."""
+               block_size=256, seqs=None, dtype="bf16"):
+        """Single-query paged decode. Returns float64 [B or len(seqs), Hq, d].
+        ``dtype`` as for :meth:`prefill_varlen`."""
         q = np.ascontiguousarray(q)
         B, Hq, d = q.shape
         kc = np.ascontiguousarray(k_cache)
@@ -167,7 +192,7 @@ class Oracle:
             out = np.zeros((n, Hq, d), dtype=np.float64)
         self._check(self.lib.oracle_decode(
             _ptr(q), _ptr(kc), _ptr(vc), num_blocks, _ptr(bt), bt.shape[1], _ptr(ctx), B, Hq,
-            num_kv_heads, d, block_size, float(scale), _ptr(seq_arr), n, _ptr(out)))
+            num_kv_heads, d, block_size, float(scale), _ptr(seq_arr), n, _elem(dtype), _ptr(out)))
         return out
 
 

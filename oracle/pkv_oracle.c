@@ -30,8 +30,12 @@
  *     Decode (flash_attn_with_kvcache) is the same with one query per
  *     sequence at position context_lens[b] - 1, i.e. keys 0..ctx-1.
  *
- * Element storage: bf16 values are passed as their raw 16-bit patterns and
- * widened exactly to double. Results are written as double.
+ * Element storage: q, k, v and the caches hold 16-bit values passed as raw
+ * bit patterns and widened exactly to double. Two element types are read:
+ * bf16 (the pages' default model dtype) and IEEE fp16 (the experiment code in
+ * "Nano-vLLM代码手撕笔记", section "目录结构概览", builds the engine with
+ * dtype=torch.float16). The store copies bit patterns and has no type.
+ * Results are written as double.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,12 +54,43 @@ enum {
     ORACLE_ERR_NOMEM = -5,
 };
 
+enum { ORACLE_ELEM_BF16 = 0, ORACLE_ELEM_F16 = 1 };
+
 /* bf16 bit pattern -> double, exact (bf16 is the top half of an fp32). */
 static double bf16_to_double(uint16_t bits) {
     uint32_t u = ((uint32_t)bits) << 16;
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* IEEE 754 binary16 bit pattern -> double, exact. Fields: sign (bit 15),
+ * exponent (bits 10-14, bias 15), fraction (bits 0-9). Exponent 0 encodes
+ * zero and subnormals, fraction * 2^-24; exponent 31 encodes infinity
+ * (fraction 0) or NaN; otherwise the value is (1024 + fraction) * 2^(e-25). */
+static double f16_to_double(uint16_t bits) {
+    int sign = (bits >> 15) & 1;
+    int e = (bits >> 10) & 0x1f;
+    int f = bits & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+static double elem_to_double(uint16_t bits, int elem) {
+    return elem == ORACLE_ELEM_F16 ? f16_to_double(bits) : bf16_to_double(bits);
+}
+
+/* Exported for the pins: widen n bit patterns of the given element type. */
+int oracle_elements_to_double(const uint16_t *bits, int64_t n, int elem, double *out) {
+    if (elem != ORACLE_ELEM_BF16 && elem != ORACLE_ELEM_F16) return -4;
+    for (int64_t i = 0; i < n; i++) out[i] = elem_to_double(bits[i], elem);
+    return 0;
 }
 
 int oracle_num_threads(void) {
@@ -98,14 +133,14 @@ int oracle_store_kvcache(const uint16_t *k, int64_t k_row_stride,
 /* krows[t] / vrows[t] point at the head_dim elements of key/value t. */
 static int attend_one_row(const double *q, const uint16_t *const *krows,
                           const uint16_t *const *vrows, int64_t n_keys,
-                          int64_t head_dim, double scale, double *out) {
+                          int64_t head_dim, double scale, int elem, double *out) {
     for (int64_t j = 0; j < head_dim; j++) out[j] = 0.0;
     if (n_keys <= 0) return ORACLE_OK;
     double *s = (double *)malloc(sizeof(double) * (size_t)n_keys);
     if (!s) return ORACLE_ERR_NOMEM;
     for (int64_t t = 0; t < n_keys; t++) {
         double dot = 0.0;
-        for (int64_t j = 0; j < head_dim; j++) dot += q[j] * bf16_to_double(krows[t][j]);
+        for (int64_t j = 0; j < head_dim; j++) dot += q[j] * elem_to_double(krows[t][j], elem);
         s[t] = scale * dot;
     }
     double m = s[0];
@@ -115,7 +150,7 @@ static int attend_one_row(const double *q, const uint16_t *const *krows,
     for (int64_t t = 0; t < n_keys; t++) {
         double w = exp(s[t] - m);
         denom += w;
-        for (int64_t j = 0; j < head_dim; j++) out[j] += w * bf16_to_double(vrows[t][j]);
+        for (int64_t j = 0; j < head_dim; j++) out[j] += w * elem_to_double(vrows[t][j], elem);
     }
     for (int64_t j = 0; j < head_dim; j++) out[j] = out[j] / denom;
     free(s);
@@ -161,6 +196,7 @@ static int gather_rows(int64_t b, int64_t hk, int64_t n_keys,
  * rows: optional list of n_rows (token, head) pairs to compute; when NULL,
  *       every (token, head) is computed and out is [total_q, Hq, head_dim].
  *       Otherwise out is [n_rows, head_dim].
+ * elem: ORACLE_ELEM_BF16 or ORACLE_ELEM_F16, the type of q, k, v and caches.
  */
 int oracle_prefill_varlen(const uint16_t *q, int64_t q_row_stride,
                           const uint16_t *k, const uint16_t *v, int64_t kv_row_stride,
@@ -169,7 +205,8 @@ int oracle_prefill_varlen(const uint16_t *q, int64_t q_row_stride,
                           const int32_t *block_tables, int64_t bt_stride,
                           int64_t num_seqs, int64_t Hq, int64_t Hkv, int64_t head_dim,
                           int64_t block_size, double scale,
-                          const int64_t *rows, int64_t n_rows, double *out) {
+                          const int64_t *rows, int64_t n_rows, int elem, double *out) {
+    if (elem != ORACLE_ELEM_BF16 && elem != ORACLE_ELEM_F16) return ORACLE_ERR_SHAPE;
     if (Hkv <= 0 || Hq % Hkv != 0 || head_dim <= 0 || block_size <= 0) return ORACLE_ERR_SHAPE;
     int64_t group = Hq / Hkv;
     int64_t total_q = cu_seqlens_q[num_seqs];
@@ -205,12 +242,12 @@ int oracle_prefill_varlen(const uint16_t *q, int64_t q_row_stride,
         if (!qd || !krows || !vrows) st = ORACLE_ERR_NOMEM;
         if (st == ORACLE_OK) {
             for (int64_t j = 0; j < head_dim; j++)
-                qd[j] = bf16_to_double(q[token * q_row_stride + h * head_dim + j]);
+                qd[j] = elem_to_double(q[token * q_row_stride + h * head_dim + j], elem);
             st = gather_rows(b, hk, n_keys, k, v, kv_row_stride, cu_seqlens_k,
                              k_cache, v_cache, num_blocks, block_tables, bt_stride,
                              Hkv, head_dim, block_size, krows, vrows);
         }
-        if (st == ORACLE_OK) st = attend_one_row(qd, krows, vrows, n_keys, head_dim, scale, o);
+        if (st == ORACLE_OK) st = attend_one_row(qd, krows, vrows, n_keys, head_dim, scale, elem, o);
         free(qd);
         free(krows);
         free(vrows);
@@ -229,13 +266,14 @@ int oracle_prefill_varlen(const uint16_t *q, int64_t q_row_stride,
  * to keys 0..context_lens[b]-1 (context_lens counts the token just stored,
  * engine/model_runner.py prepare_decode appends len(seq)).
  * seqs: optional subset of n_seqs sequence indices; out is
- * [n_seqs or num_seqs, Hq, head_dim].
+ * [n_seqs or num_seqs, Hq, head_dim]. elem as for prefill.
  */
 int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                   int64_t num_blocks, const int32_t *block_tables, int64_t bt_stride,
                   const int32_t *context_lens, int64_t num_seqs, int64_t Hq, int64_t Hkv,
                   int64_t head_dim, int64_t block_size, double scale,
-                  const int64_t *seqs, int64_t n_seqs, double *out) {
+                  const int64_t *seqs, int64_t n_seqs, int elem, double *out) {
+    if (elem != ORACLE_ELEM_BF16 && elem != ORACLE_ELEM_F16) return ORACLE_ERR_SHAPE;
     if (Hkv <= 0 || Hq % Hkv != 0 || head_dim <= 0 || block_size <= 0) return ORACLE_ERR_SHAPE;
     if (!block_tables) return ORACLE_ERR_SHAPE;
     int64_t group = Hq / Hkv;
@@ -263,11 +301,11 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
         if (!qd || !krows || !vrows) st = ORACLE_ERR_NOMEM;
         if (st == ORACLE_OK) {
             for (int64_t j = 0; j < head_dim; j++)
-                qd[j] = bf16_to_double(q[(b * Hq + h) * head_dim + j]);
+                qd[j] = elem_to_double(q[(b * Hq + h) * head_dim + j], elem);
             st = gather_rows(b, hk, n_keys, NULL, NULL, 0, NULL, k_cache, v_cache, num_blocks,
                              block_tables, bt_stride, Hkv, head_dim, block_size, krows, vrows);
         }
-        if (st == ORACLE_OK) st = attend_one_row(qd, krows, vrows, n_keys, head_dim, scale, o);
+        if (st == ORACLE_OK) st = attend_one_row(qd, krows, vrows, n_keys, head_dim, scale, elem, o);
         free(qd);
         free(krows);
         free(vrows);

@@ -42,6 +42,20 @@ def randn_bits(rng, shape, scale=1.0):
     return bf16_bits(rng.standard_normal(shape).astype(np.float32) * scale)
 
 
+def f16_bits(x: np.ndarray) -> np.ndarray:
+    """float array -> IEEE fp16 bit patterns (numpy's round to nearest even)."""
+    return np.ascontiguousarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.float16)
+    return t.double().numpy()
+
+
+def randn_f16_bits(rng, shape, scale=1.0):
+    return f16_bits(rng.standard_normal(shape) * scale)
+
+
 def paged_from_contiguous(k, v, cu_k, rng, num_blocks, bs=BS, fill=None):
     """Scatter contiguous per-sequence K/V into a shuffled paged pool.
 
@@ -76,14 +90,16 @@ def paged_from_contiguous(k, v, cu_k, rng, num_blocks, bs=BS, fill=None):
     return kc.reshape(num_blocks, bs, hkv, d), vc.reshape(num_blocks, bs, hkv, d), bt
 
 
-def sdpa_reference(q, k, v, cu_q, cu_k, scale):
+def sdpa_reference(q, k, v, cu_q, cu_k, scale, widen=None):
     """torch SDPA (float64, CPU) per sequence, bottom-right causal mask given
-    as an explicit boolean matrix, GQA through enable_gqa."""
+    as an explicit boolean matrix, GQA through enable_gqa. ``widen`` turns bit
+    patterns into float64 (bf16 by default)."""
+    widen = bits_to_f64 if widen is None else widen
     outs = []
     for b in range(len(cu_q) - 1):
-        qb = torch.from_numpy(bits_to_f64(q[cu_q[b]:cu_q[b + 1]])).transpose(0, 1)   # [Hq, Lq, d]
-        kb = torch.from_numpy(bits_to_f64(k[cu_k[b]:cu_k[b + 1]])).transpose(0, 1)   # [Hkv, Lk, d]
-        vb = torch.from_numpy(bits_to_f64(v[cu_k[b]:cu_k[b + 1]])).transpose(0, 1)
+        qb = torch.from_numpy(widen(q[cu_q[b]:cu_q[b + 1]])).transpose(0, 1)   # [Hq, Lq, d]
+        kb = torch.from_numpy(widen(k[cu_k[b]:cu_k[b + 1]])).transpose(0, 1)   # [Hkv, Lk, d]
+        vb = torch.from_numpy(widen(v[cu_k[b]:cu_k[b + 1]])).transpose(0, 1)
         lq, lk = qb.shape[1], kb.shape[1]
         mask = torch.ones(lq, lk, dtype=torch.bool).tril(diagonal=lk - lq)
         o = F.scaled_dot_product_attention(qb[None], kb[None], vb[None], attn_mask=mask, scale=scale,
@@ -345,6 +361,59 @@ def pin_store_layout(orc):
             assert np.all(kc[s] == 0x7FC0) and np.all(vc[s] == 0x7FC0)
 
 
+def pin_element_widening(orc):
+    """Every one of the 65536 bit patterns widens exactly as numpy reads it:
+    bf16 as the top half of an IEEE float32, fp16 as IEEE binary16 (zeros
+    with their sign, subnormals, infinities, NaNs)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):     # signalling-NaN patterns widen to quiet NaNs
+        want_bf16 = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        want_f16 = bits.view(np.float16).astype(np.float64)
+    for dtype, want in (("bf16", want_bf16), ("f16", want_f16)):
+        got = orc.elements_to_f64(bits, dtype)
+        np.testing.assert_array_equal(got, want)
+        fin = np.isfinite(want)
+        assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+
+
+def pin_sdpa_f16_prefix(orc):
+    """fp16 inputs: prefix-cache prefill against float64 SDPA on the same
+    fp16 values read by torch. One sequence's keys are tiny (fp16
+    subnormals) and another's values large (|v| up to thousands), so both
+    ends of the fp16 range are decoded."""
+    rng = np.random.default_rng(25)
+    lq, lk = [6, 30, 2], [270, 30, 520]
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    q = randn_f16_bits(rng, (int(cu_q[-1]), 4, 128))
+    kf = rng.standard_normal((int(cu_k[-1]), 2, 128))
+    kf[cu_k[1]:cu_k[2]] *= 3e-6                    # fp16 subnormal range (< 6.1e-5)
+    vf = rng.standard_normal((int(cu_k[-1]), 2, 128))
+    vf[cu_k[2]:] *= 2000.0
+    k, v = f16_bits(kf), f16_bits(vf)
+    kc, vc, bt = paged_from_contiguous(k, v, cu_k, rng, num_blocks=9)
+    scale = 1 / math.sqrt(128)
+    got = orc.prefill_varlen(q, cu_q, cu_k, scale, k_cache=kc, v_cache=vc, block_tables=bt,
+                             num_kv_heads=2, dtype="f16")
+    ref = sdpa_reference(q, k, v, cu_q, cu_k, scale, widen=f16_bits_to_f64)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_decode_sdpa_f16(orc):
+    """fp16 decode against float64 SDPA on the contiguous keys."""
+    rng = np.random.default_rng(26)
+    ctx = np.array([2, 257, 600], dtype=np.int32)
+    cu = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
+    k = randn_f16_bits(rng, (int(ctx.sum()), 2, 128))
+    v = randn_f16_bits(rng, (int(ctx.sum()), 2, 128), scale=10.0)
+    q = randn_f16_bits(rng, (len(ctx), 4, 128))
+    kc, vc, bt = paged_from_contiguous(k, v, cu, rng, num_blocks=7)
+    got = orc.decode(q, kc, vc, bt, ctx, 0.0884, num_kv_heads=2, dtype="f16")
+    cuq = np.arange(len(ctx) + 1, dtype=np.int32)
+    ref = sdpa_reference(q, k, v, cuq, cu, 0.0884, widen=f16_bits_to_f64)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
 ALL_PINS = [
     pin_sdpa_equal_lengths,
     pin_sdpa_prefix,
@@ -361,4 +430,7 @@ ALL_PINS = [
     pin_decode_empty_context,
     pin_shared_prefix,
     pin_store_layout,
+    pin_element_widening,
+    pin_sdpa_f16_prefix,
+    pin_decode_sdpa_f16,
 ]

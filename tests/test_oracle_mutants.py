@@ -21,7 +21,7 @@ MUTANTS = [
     ("max subtracted with the wrong sign", "double w = exp(s[t] - m);", "double w = exp(m - s[t]);"),
     ("normalisation dropped", "out[j] = out[j] / denom;", "out[j] = out[j] / (double)n_keys;"),
     ("value operand read from keys",
-     "out[j] += w * bf16_to_double(vrows[t][j]);", "out[j] += w * bf16_to_double(krows[t][j]);"),
+     "out[j] += w * elem_to_double(vrows[t][j], elem);", "out[j] += w * elem_to_double(krows[t][j], elem);"),
     ("in-block offset transposed", "int64_t slot = block * block_size + t % block_size;",
      "int64_t slot = block * block_size + t / block_size;"),
     ("head offset dropped in gather", "krows[t] = k_cache + slot * D + hk * head_dim;",
@@ -30,8 +30,15 @@ MUTANTS = [
      "k_cache[slot * D + e] = k[i * D + e];"),
     ("decode context excludes the new token", "int64_t n_keys = context_lens[b];",
      "int64_t n_keys = context_lens[b] - 1;"),
-    ("query read from the wrong head", "qd[j] = bf16_to_double(q[token * q_row_stride + h * head_dim + j]);",
-     "qd[j] = bf16_to_double(q[token * q_row_stride + hk * head_dim + j]);"),
+    ("query read from the wrong head", "qd[j] = elem_to_double(q[token * q_row_stride + h * head_dim + j], elem);",
+     "qd[j] = elem_to_double(q[token * q_row_stride + hk * head_dim + j], elem);"),
+    ("fp16 exponent bias off by one", "v = ldexp((double)(1024 + f), e - 25);",
+     "v = ldexp((double)(1024 + f), e - 24);"),
+    ("fp16 implicit leading one dropped", "v = ldexp((double)(1024 + f), e - 25);",
+     "v = ldexp((double)f, e - 15);"),
+    ("fp16 subnormal scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -14);"),
+    ("fp16 read as bf16", "return elem == ORACLE_ELEM_F16 ? f16_to_double(bits) : bf16_to_double(bits);",
+     "return bf16_to_double(bits);"),
 ]
 
 _CHILD = r"""
