@@ -142,20 +142,20 @@ def job_throughput(units_per_rank, world, ms_step):
 # the decode step (ours)
 # ---------------------------------------------------------------------------
 
-def decode_case(pkv, dev, seed=2):
+def decode_case(pkv, dev, seed=2, dtype=torch.bfloat16):
     wl = W.batched_decode(seed=seed)
     gen = W.make_generator(seed, dev)
     shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
-    kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
+    kc, vc = W.normal(shape, gen, dev, dtype), W.normal(shape, gen, dev, dtype)
     B = len(wl.seqs)
-    qkv, q, k, v = W.fused_qkv(B, gen, dev)
+    qkv, q, k, v = W.fused_qkv(B, gen, dev, dtype=dtype)
     meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE, table_width=W.MAX_MODEL_LEN // W.BLOCK_SIZE)
     c = dict(wl=wl, kc=kc, vc=vc, qkv=qkv, q=q, k=k, v=v, meta=meta, B=B,
              slot=torch.from_numpy(meta["slot_mapping"]).to(dev),
              ctx=torch.from_numpy(meta["context_lens"]).to(dev),
              bt=torch.from_numpy(meta["block_tables"]).to(dev),
              ws=pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev),
-             out=torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev))
+             out=torch.empty(B, W.HQ, W.HEAD_DIM, dtype=dtype, device=dev))
     ctx = meta["context_lens"].astype(np.int64)
     c["kv_bytes"] = int(ctx.sum()) * W.HKV * W.HEAD_DIM * 2 * 2
     c["decode_alg_bytes"] = (c["kv_bytes"] + B * W.HQ * W.HEAD_DIM * 2 * 2 + meta["block_tables"].nbytes
@@ -227,6 +227,8 @@ def run_ours(args, rank, world, dev):
         res["prefill"] = run_prefill(pkv, args, dev, bf16)
     if rank == 0 and not args.no_sweep:
         res["sweep"] = run_sweep(pkv, args, dev, hbm)
+    if rank == 0 and not args.no_f16:
+        res["f16"] = run_f16(pkv, args, dev, hbm, bf16)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(c, budget_s=args.cpu_seconds)
     return res
@@ -277,7 +279,9 @@ def _prefill_flops(seqs):
     return 4 * W.HEAD_DIM * W.HQ * tot
 
 
-def run_prefill(pkv, args, dev, bf16_peak):
+def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
+    f16 = dtype == torch.float16
+    prefill = pkv.pkv_prefill_varlen_f16 if f16 else pkv.pkv_prefill_varlen
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     res = {}
     iters = max(3, min(args.steps, 20))
@@ -285,11 +289,11 @@ def run_prefill(pkv, args, dev, bf16_peak):
                      ("prefix_prefill_128s_prefix1024_suffix64-512", W.prefix_prefill())):
         gen = W.make_generator(wl.seed, dev)
         shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
-        kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
+        kc, vc = W.normal(shape, gen, dev, dtype), W.normal(shape, gen, dev, dtype)
         calls = []
         for seqs in wl.seqs:
             T = sum(s.num_scheduled_tokens for s in seqs)
-            _, q, k, v = W.fused_qkv(T, gen, dev)
+            _, q, k, v = W.fused_qkv(T, gen, dev, dtype=dtype)
             m = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
             calls.append(dict(q=q, k=k, v=v, m=m, T=T, flops=_prefill_flops(seqs),
                               slot=torch.from_numpy(m["slot_mapping"]).to(dev),
@@ -304,8 +308,8 @@ def run_prefill(pkv, args, dev, bf16_peak):
                 e0.record()
                 pkv.pkv_store_kvcache(cl["k"], cl["v"], kc, vc, cl["slot"])
                 e1.record()
-                pkv.pkv_prefill_varlen(cl["q"], cl["cq"], cl["ck"], cl["m"]["max_seqlen_q"], cl["m"]["max_seqlen_k"],
-                                       W.SCALE, k_cache=kc, v_cache=vc, block_tables=cl["bt"])
+                prefill(cl["q"], cl["cq"], cl["ck"], cl["m"]["max_seqlen_q"], cl["m"]["max_seqlen_k"],
+                        W.SCALE, k_cache=kc, v_cache=vc, block_tables=cl["bt"])
                 e2.record()
                 if it >= 3:
                     cl.setdefault("ev", []).append((e0, e1, e2))
@@ -319,11 +323,43 @@ def run_prefill(pkv, args, dev, bf16_peak):
                      "prefill_ms": round(t_pre, 4), "tflops": round(tf, 1),
                      "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(tf, 1),
                                   "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
-                                  "peak_source": "measured bf16 dense (cuBLAS burst)",
-                                  "traffic": _traffic("prefill.cu", flops)},
+                                  "peak_source": ("measured bf16 dense (cuBLAS burst) x nominal fp16/bf16 ratio 1"
+                                                  if f16 else "measured bf16 dense (cuBLAS burst)"),
+                                  "traffic": None if f16 else _traffic("prefill.cu", flops)},
                      "store_ms": round(t_st, 4), "store_gbs": round(store_bytes / (t_st * 1e-3) / 1e9, 1),
                      "l2": "256 MB buffer written between launches"}
     assert pkv.pkv_device_error() == 0
+    return res
+
+
+def run_f16(pkv, args, dev, hbm_peak, bf16_peak):
+    """The fp16 entry points on the same workloads: decode (store + decode of
+    the 256-sequence batch, kernel time by CUDA events) and both prefill cases."""
+    c = decode_case(pkv, dev, dtype=torch.float16)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 50))
+    evs = []
+    for it in range(args.warmup + steps):
+        pkv.pkv_store_kvcache(c["k"], c["v"], c["kc"], c["vc"], c["slot"])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkv.pkv_decode_f16(c["q"], c["kc"], c["vc"], c["bt"], c["ctx"], W.MAX_MODEL_LEN, W.SCALE, c["ws"],
+                           out=c["out"])
+        e1.record(stream)
+        if it >= args.warmup:
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    ach = c["decode_alg_bytes"] / (dec_ms * 1e-3) / 1e9
+    if pkv.pkv_device_error():
+        raise RuntimeError("device error word set by the fp16 decode")
+    res = {"decode": {"workload": "batched_decode_b256_ctx512-4096 (fp16)", "avg_launch_ms": round(dec_ms, 5),
+                      "roofline": {"kernel": "decode_split_kernel<fp16>", "bound": "hbm", "achieved": round(ach, 1),
+                                   "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                                   "traffic": None}}}
+    del c
+    if not args.no_prefill:
+        res["prefill"] = run_prefill(pkv, args, dev, bf16_peak, dtype=torch.float16)
     return res
 
 
@@ -542,6 +578,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-sample", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-f16", action="store_true", help="skip the fp16 entry points' timings")
     ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "store"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

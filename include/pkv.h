@@ -11,7 +11,11 @@
  *     and "请求执行 – run model" (the same steps with a worked example).
  *
  * Conventions shared by every entry point
- *   - Element type: bf16 for q, k, v, caches and outputs. Index arrays int32.
+ *   - Element type: bf16 for q, k, v, caches and outputs; the *_f16 entry
+ *     points take IEEE fp16 for all of them instead (the experiment code in
+ *     "Nano-vLLM代码手撕笔记", section "目录结构概览", builds the engine with
+ *     dtype=torch.float16). Arithmetic is fp32 for both. pkv_store_kvcache
+ *     copies 16-bit patterns and serves both types. Index arrays int32.
  *   - Supported shape: head_dim = 128, block_size = 256; prefill and decode
  *     also need num_kv_heads = 8 and num_heads = 16 (Qwen3-0.6B attention:
  *     16 query heads grouped 2 per kv head). Query head h reads kv head
@@ -79,11 +83,12 @@ int pkv_version(void);
  * (num_kv_heads*head_dim elements each, a bit-exact copy). Tokens with
  * slot -1 (padding) are skipped.
  *
- *   k, v            [num_tokens, num_kv_heads, head_dim] bf16; heads and
+ *   k, v            [num_tokens, num_kv_heads, head_dim] 16-bit elements
+ *                   (bf16 or fp16: the copy is bit-exact either way); heads and
  *                   dims contiguous within a row, rows k_row_stride /
  *                   v_row_stride ELEMENTS apart (>= num_kv_heads*head_dim;
  *                   e.g. 4096 for views of a fused qkv projection).
- *   k_cache,v_cache [num_slots, num_kv_heads, head_dim] bf16, contiguous
+ *   k_cache,v_cache [num_slots, num_kv_heads, head_dim], same type, contiguous
  *                   (num_slots = num_blocks * block_size).
  *   slot_mapping    [num_tokens] int32.
  * Any head_dim and num_kv_heads are accepted. When every pointer is 16-byte
@@ -139,7 +144,21 @@ int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, con
                        int32_t block_size, float softmax_scale, void* out, void* workspace,
                        size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes pkv_prefill_varlen needs for these sizes (may be 0). */
+/*
+ * pkv_prefill_varlen_f16 -- pkv_prefill_varlen with IEEE fp16 q, k, v,
+ * caches and output (fp32 logits and accumulation; P is rounded to fp16
+ * for the probability-times-value product). Arguments, layouts and errors
+ * as for pkv_prefill_varlen.
+ */
+int pkv_prefill_varlen_f16(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                           int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                           int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_tables,
+                           int32_t block_table_stride, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, float softmax_scale, void* out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes pkv_prefill_varlen(_f16) needs for these sizes (may be 0). */
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
 
 /*
@@ -196,7 +215,25 @@ int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t
                      int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes pkv_decode needs for these sizes. */
+/*
+ * pkv_decode_f16 / pkv_store_decode_f16 -- pkv_decode and pkv_store_decode
+ * with IEEE fp16 q, k, v, caches and output (fp32 arithmetic). Arguments,
+ * layouts, workspace and errors as for the bf16 calls; a workspace may be
+ * shared between bf16 and fp16 calls under the same ordering rule.
+ */
+int pkv_decode_f16(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                   int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                   const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int pkv_store_decode_f16(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                         int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                         int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale,
+                         void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes pkv_decode, pkv_store_decode and their _f16 forms need for these sizes. */
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len);
 
 /*

@@ -8,10 +8,12 @@ fails loudly when ``libpkv.so`` has not been built
 (``python paged_kv_cache_kvh_gb300/build_lib.py``).
 
 Layouts (Qwen3-0.6B attention shape):
-  q            [tokens, 16, 128] bf16 (row stride may exceed 2048, e.g. fused qkv)
-  k, v         [tokens, 8, 128]  bf16
-  k/v caches   [num_blocks, 256, 8, 128] bf16 contiguous
+  q            [tokens, 16, 128] (row stride may exceed 2048, e.g. fused qkv)
+  k, v         [tokens, 8, 128]
+  k/v caches   [num_blocks, 256, 8, 128] contiguous
   slot_mapping, cu_seqlens_*, block_tables, context_lens  int32 on the GPU
+Element type: bf16 for the plain names, fp16 for the ``*_f16`` names (one type
+per call for q, k, v, caches and output); the store copies either.
 """
 from __future__ import annotations
 
@@ -51,6 +53,13 @@ _SIGNATURES = {
     "pkv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _vp, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pkv_prefill_varlen_f16": (ctypes.c_int, [_vp, _i64, _i32, _vp, _vp, _i64, _i32, _vp, _vp, _i32, _vp, _vp, _i32,
+                                              _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
+                                              _vp]),
+    "pkv_decode_f16": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                      _f32, _vp, _vp, _sz, _vp]),
+    "pkv_store_decode_f16": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp,
+                                            _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "pkv_store_decode": (ctypes.c_int, [_vp, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _i32,
                                         _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, _vp]),
     "pkv_decode_noalloc": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
@@ -107,22 +116,33 @@ def _dev_i32(t, name):
     _need(t.dtype == torch.int32 and t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous int32 CUDA tensor")
 
 
-def _rows(t, name, heads):
-    _need(t.dtype == torch.bfloat16 and t.is_cuda, f"{name} must be a bf16 CUDA tensor")
+_TYPE_NAME = {torch.bfloat16: "bf16", torch.float16: "fp16"}
+
+
+def _rows(t, name, heads, dtype=torch.bfloat16):
+    _need(t.dtype == dtype and t.is_cuda, f"{name} must be a {_TYPE_NAME[dtype]} CUDA tensor")
     _need(t.dim() == 3 and t.shape[1] == heads and t.shape[2] == HEAD_DIM, f"{name} must be [N, {heads}, 128]")
     _need(t.stride(2) == 1 and t.stride(1) == HEAD_DIM, f"{name}: heads and dims must be contiguous within a row")
 
 
+def _cache(t, name, dtype):
+    _need(t is not None and t.dtype == dtype and t.is_cuda and t.is_contiguous()
+          and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM),
+          f"{name}: contiguous {_TYPE_NAME[dtype]} [blocks, 256, 8, 128]")
+
+
 def pkv_store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
-    """store_kvcache: k_cache[slot] = k[i], v_cache[slot] = v[i] for slot != -1."""
+    """store_kvcache: k_cache[slot] = k[i], v_cache[slot] = v[i] for slot != -1.
+    A bit-exact copy of 16-bit elements: bf16 or fp16, the same type throughout."""
     _need(k.dim() == 3 and v.shape == k.shape, "k, v must be [N, num_kv_heads, head_dim]")
     N, hkv, d = k.shape
+    _need(k.dtype in _TYPE_NAME, "k, v, caches must be bf16 or fp16")
     for t, n in ((k, "k"), (v, "v")):
-        _need(t.dtype == torch.bfloat16 and t.is_cuda and t.stride(2) == 1 and t.stride(1) == d,
-              f"{n}: bf16 CUDA, heads and dims contiguous")
+        _need(t.dtype == k.dtype and t.is_cuda and t.stride(2) == 1 and t.stride(1) == d,
+              f"{n}: CUDA, same type as k, heads and dims contiguous")
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t.dtype == torch.bfloat16 and t.is_contiguous() and t.shape[-2:] == (hkv, d),
-              f"{n}: contiguous bf16 [..., {hkv}, {d}]")
+        _need(t.dtype == k.dtype and t.is_contiguous() and t.shape[-2:] == (hkv, d),
+              f"{n}: contiguous, same type as k, [..., {hkv}, {d}]")
     _dev_i32(slot_mapping, "slot_mapping")
     _need(slot_mapping.numel() == N, "slot_mapping must have one entry per token")
     num_slots = k_cache.numel() // (hkv * d)
@@ -134,46 +154,59 @@ def pkv_prefill_workspace_bytes(num_seqs: int, max_seqlen_q: int, num_heads: int
     return int(_lib.pkv_prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads))
 
 
-def pkv_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, *, k=None, v=None,
-                       k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None, stream=None):
-    """flash_attn_varlen_func(q, k, v, ..., causal=True, block_table=block_tables).
-
-    Paged keys (k_cache/v_cache through block_tables) when block_tables is
-    given, else contiguous k/v. Returns out [total_q, 16, 128] bf16."""
-    _rows(q, "q", NUM_HEADS)
+def _prefill(entry, dtype, q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, k, v,
+             k_cache, v_cache, block_tables, out, workspace, stream):
+    _rows(q, "q", NUM_HEADS, dtype)
     _dev_i32(cu_seqlens_q, "cu_seqlens_q")
     _dev_i32(cu_seqlens_k, "cu_seqlens_k")
     num_seqs = cu_seqlens_q.numel() - 1
     _need(cu_seqlens_k.numel() == num_seqs + 1, "cu_seqlens_k size")
     total_q = q.shape[0]
     if out is None:
-        out = torch.empty((total_q, NUM_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
-    _need(out.is_contiguous() and out.shape == (total_q, NUM_HEADS, HEAD_DIM) and out.dtype == torch.bfloat16,
-          "out must be contiguous bf16 [total_q, 16, 128]")
+        out = torch.empty((total_q, NUM_HEADS, HEAD_DIM), dtype=dtype, device=q.device)
+    _need(out.is_contiguous() and out.shape == (total_q, NUM_HEADS, HEAD_DIM) and out.dtype == dtype,
+          f"out must be contiguous {_TYPE_NAME[dtype]} [total_q, 16, 128]")
     if block_tables is not None:
         _dev_i32(block_tables, "block_tables")
-        for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-            _need(t is not None and t.dtype == torch.bfloat16 and t.is_contiguous()
-                  and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+        _cache(k_cache, "k_cache", dtype)
+        _cache(v_cache, "v_cache", dtype)
         num_blocks, bt_stride = k_cache.shape[0], block_tables.shape[1]
         kk = vv = None
         kv_stride, total_k = 0, 0
     else:
-        _rows(k, "k", NUM_KV_HEADS)
-        _rows(v, "v", NUM_KV_HEADS)
+        _rows(k, "k", NUM_KV_HEADS, dtype)
+        _rows(v, "v", NUM_KV_HEADS, dtype)
         _need(k.stride(0) == v.stride(0) and k.shape == v.shape, "k and v must share shape and row stride")
         kk, vv = k, v
         kv_stride, total_k = k.stride(0), k.shape[0]
         num_blocks, bt_stride = 0, 0
-    ws_bytes = pkv_prefill_workspace_bytes(num_seqs, int(max_seqlen_q))
-    _check(_lib.pkv_prefill_varlen(
+    fn = getattr(_lib, entry)
+    _check(fn(
         _ptr(q), q.stride(0), total_q, _ptr(kk), _ptr(vv), kv_stride, total_k,
         _ptr(k_cache) if block_tables is not None else None, _ptr(v_cache) if block_tables is not None else None,
         num_blocks, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k),
         _ptr(block_tables), bt_stride, num_seqs, NUM_HEADS, NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE,
         float(softmax_scale), _ptr(out), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        _stream(stream)), "pkv_prefill_varlen")
+        _stream(stream)), entry)
     return out
+
+
+def pkv_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, *, k=None, v=None,
+                       k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None, stream=None):
+    """flash_attn_varlen_func(q, k, v, ..., causal=True, block_table=block_tables).
+
+    Paged keys (k_cache/v_cache through block_tables) when block_tables is
+    given, else contiguous k/v. Returns out [total_q, 16, 128] bf16."""
+    return _prefill("pkv_prefill_varlen", torch.bfloat16, q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    softmax_scale, k, v, k_cache, v_cache, block_tables, out, workspace, stream)
+
+
+def pkv_prefill_varlen_f16(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, *, k=None,
+                           v=None, k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None,
+                           stream=None):
+    """pkv_prefill_varlen on fp16 tensors; returns fp16."""
+    return _prefill("pkv_prefill_varlen_f16", torch.float16, q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                    max_seqlen_k, softmax_scale, k, v, k_cache, v_cache, block_tables, out, workspace, stream)
 
 
 def pkv_decode_workspace_bytes(num_seqs: int, max_context_len: int, num_heads: int = NUM_HEADS) -> int:
@@ -186,27 +219,40 @@ def decode_workspace(num_seqs: int, max_context_len: int, device="cuda") -> torc
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
-def pkv_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale, workspace, *,
-               out=None, stream=None):
-    """flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens=context_lens,
-    block_table=block_tables, causal=True). Returns out [num_seqs, 16, 128] bf16."""
-    _rows(q, "q", NUM_HEADS)
-    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t.dtype == torch.bfloat16 and t.is_contiguous()
-              and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+def _decode(entry, dtype, q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale,
+            workspace, out, stream):
+    _rows(q, "q", NUM_HEADS, dtype)
+    _cache(k_cache, "k_cache", dtype)
+    _cache(v_cache, "v_cache", dtype)
     _dev_i32(block_tables, "block_tables")
     _dev_i32(context_lens, "context_lens")
     B = q.shape[0]
     _need(block_tables.dim() == 2 and block_tables.shape[0] >= B and context_lens.numel() >= B, "table sizes")
     if out is None:
-        out = torch.empty((B, NUM_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
-    _need(out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM), "out must be contiguous [B, 16, 128]")
+        out = torch.empty((B, NUM_HEADS, HEAD_DIM), dtype=dtype, device=q.device)
+    _need(out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM) and out.dtype == dtype,
+          f"out must be contiguous {_TYPE_NAME[dtype]} [B, 16, 128]")
     _need(workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace must be a uint8 CUDA tensor")
-    _check(_lib.pkv_decode(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
-                           _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
-                           NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
-                           _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_decode")
+    _check(getattr(_lib, entry)(_ptr(q), q.stride(0), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
+                                NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
+                                _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), entry)
     return out
+
+
+def pkv_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale, workspace, *,
+               out=None, stream=None):
+    """flash_attn_with_kvcache(q.unsqueeze(1), k_cache, v_cache, cache_seqlens=context_lens,
+    block_table=block_tables, causal=True). Returns out [num_seqs, 16, 128] bf16."""
+    return _decode("pkv_decode", torch.bfloat16, q, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                   softmax_scale, workspace, out, stream)
+
+
+def pkv_decode_f16(q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale, workspace, *,
+                   out=None, stream=None):
+    """pkv_decode on fp16 tensors; returns fp16."""
+    return _decode("pkv_decode_f16", torch.float16, q, k_cache, v_cache, block_tables, context_lens,
+                   max_context_len, softmax_scale, workspace, out, stream)
 
 
 def pkv_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len, softmax_scale, out, *,
@@ -219,9 +265,8 @@ def pkv_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_cont
     (PKV_DECODE_NOALLOC_SCRATCH_BYTES) raise PkvError(PKV_ERR_SCRATCH_LIMIT).
     Calls must not overlap on the GPU: they share the array."""
     _rows(q, "q", NUM_HEADS)
-    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t.dtype == torch.bfloat16 and t.is_contiguous()
-              and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+    _cache(k_cache, "k_cache", torch.bfloat16)
+    _cache(v_cache, "v_cache", torch.bfloat16)
     _dev_i32(block_tables, "block_tables")
     _dev_i32(context_lens, "context_lens")
     B = q.shape[0]
@@ -235,16 +280,13 @@ def pkv_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_cont
     return out
 
 
-def pkv_store_decode(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, max_context_len,
-                     softmax_scale, workspace, *, out=None, stream=None):
-    """store_kvcache of the step's new K/V rows fused into the decode launch.
-    slot_mapping[b] must be -1 or the slot of position context_lens[b]-1."""
-    _rows(q, "q", NUM_HEADS)
-    _rows(k, "k", NUM_KV_HEADS)
-    _rows(v, "v", NUM_KV_HEADS)
-    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t.dtype == torch.bfloat16 and t.is_contiguous()
-              and tuple(t.shape[1:]) == (BLOCK_SIZE, NUM_KV_HEADS, HEAD_DIM), f"{n}: [blocks, 256, 8, 128]")
+def _store_decode(entry, dtype, q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+                  max_context_len, softmax_scale, workspace, out, stream):
+    _rows(q, "q", NUM_HEADS, dtype)
+    _rows(k, "k", NUM_KV_HEADS, dtype)
+    _rows(v, "v", NUM_KV_HEADS, dtype)
+    _cache(k_cache, "k_cache", dtype)
+    _cache(v_cache, "v_cache", dtype)
     _dev_i32(slot_mapping, "slot_mapping")
     _dev_i32(block_tables, "block_tables")
     _dev_i32(context_lens, "context_lens")
@@ -252,15 +294,31 @@ def pkv_store_decode(q, k, v, slot_mapping, k_cache, v_cache, block_tables, cont
     _need(k.shape[0] >= B and v.shape[0] >= B and slot_mapping.numel() >= B, "one new row per sequence")
     _need(block_tables.dim() == 2 and block_tables.shape[0] >= B and context_lens.numel() >= B, "table sizes")
     if out is None:
-        out = torch.empty((B, NUM_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
-    _need(out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM), "out must be contiguous [B, 16, 128]")
+        out = torch.empty((B, NUM_HEADS, HEAD_DIM), dtype=dtype, device=q.device)
+    _need(out.is_contiguous() and out.shape == (B, NUM_HEADS, HEAD_DIM) and out.dtype == dtype,
+          f"out must be contiguous {_TYPE_NAME[dtype]} [B, 16, 128]")
     _need(workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace must be a uint8 CUDA tensor")
-    _check(_lib.pkv_store_decode(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(v), v.stride(0),
-                                 _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
-                                 _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
-                                 NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
-                                 _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), "pkv_store_decode")
+    _check(getattr(_lib, entry)(_ptr(q), q.stride(0), _ptr(k), k.stride(0), _ptr(v), v.stride(0),
+                                _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), B, NUM_HEADS,
+                                NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE, int(max_context_len), float(softmax_scale),
+                                _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)), entry)
     return out
+
+
+def pkv_store_decode(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                     softmax_scale, workspace, *, out=None, stream=None):
+    """store_kvcache of the step's new K/V rows fused into the decode launch.
+    slot_mapping[b] must be -1 or the slot of position context_lens[b]-1."""
+    return _store_decode("pkv_store_decode", torch.bfloat16, q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                         context_lens, max_context_len, softmax_scale, workspace, out, stream)
+
+
+def pkv_store_decode_f16(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                         softmax_scale, workspace, *, out=None, stream=None):
+    """pkv_store_decode on fp16 tensors; returns fp16."""
+    return _store_decode("pkv_store_decode_f16", torch.float16, q, k, v, slot_mapping, k_cache, v_cache,
+                         block_tables, context_lens, max_context_len, softmax_scale, workspace, out, stream)
 
 
 def pkv_build_prefill_metadata(num_cached_tokens, num_scheduled_tokens, block_tables, num_blocks, capacity,

@@ -22,6 +22,8 @@
 //    Sequences with a single block write the output directly.
 //  * Logits are kept in the log2 domain (q is pre-scaled by scale*log2(e))
 //    and exponentials use ex2.approx.
+//  * The element type (bf16 or fp16) is a template parameter: it only changes
+//    how packed pairs are widened to fp32 and how the output is rounded.
 #include "pkv_common.cuh"
 
 #ifndef PKV_DECODE_TOKENS_PER_STAGE
@@ -52,7 +54,7 @@ constexpr int kConsumerWarps = kHkv;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 struct DecodeParams {
-  const __nv_bfloat16* q;
+  const uint16_t* q;  // 16-bit elements of the call's type
   int64_t q_row_stride;
   const uint8_t* k_cache;
   const uint8_t* v_cache;
@@ -63,7 +65,7 @@ struct DecodeParams {
   int32_t max_ctx;
   int32_t nsplit;
   float scale_log2;
-  __nv_bfloat16* out;
+  uint16_t* out;
   int32_t* tickets;   // [num_seqs]
   float2* ml;         // [num_seqs, nsplit, 16] (running max in log2 units, sum)
   float* opart;       // [num_seqs, nsplit, 16, 128] unnormalised partial outputs
@@ -112,9 +114,10 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
   return v[0];
 }
 
-template <int kT, int kStages>
+template <Elem E, int kT, int kStages>
 __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100 * 1024) ? 2 : 1)
     decode_split_kernel(const DecodeParams p) {
+  using Ops = ElemOps<E>;
   static_assert(2 * kT <= 32 && (kT & (kT - 1)) == 0, "kT must be a power of two <= 16");
   constexpr int kStageBytes = 2 * kT * kRowBytes;
   constexpr int kN = 2 * kT;                 // logits per warp per stage
@@ -210,17 +213,17 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
     // ---------------- consumers: warp h = kv head h, query heads 2h, 2h+1 ----------------
     float q0[4], q1[4];
     {
-      const __nv_bfloat16* qrow = p.q + static_cast<int64_t>(b) * p.q_row_stride;
+      const uint16_t* qrow = p.q + static_cast<int64_t>(b) * p.q_row_stride;
       const uint2 a = *reinterpret_cast<const uint2*>(qrow + (kGroup * h) * kHeadDim + lane * 4);
       const uint2 bq = *reinterpret_cast<const uint2*>(qrow + (kGroup * h + 1) * kHeadDim + lane * 4);
-      q0[0] = bf16lo_to_f32(a.x) * p.scale_log2;
-      q0[1] = bf16hi_to_f32(a.x) * p.scale_log2;
-      q0[2] = bf16lo_to_f32(a.y) * p.scale_log2;
-      q0[3] = bf16hi_to_f32(a.y) * p.scale_log2;
-      q1[0] = bf16lo_to_f32(bq.x) * p.scale_log2;
-      q1[1] = bf16hi_to_f32(bq.x) * p.scale_log2;
-      q1[2] = bf16lo_to_f32(bq.y) * p.scale_log2;
-      q1[3] = bf16hi_to_f32(bq.y) * p.scale_log2;
+      q0[0] = Ops::lo(a.x) * p.scale_log2;
+      q0[1] = Ops::hi(a.x) * p.scale_log2;
+      q0[2] = Ops::lo(a.y) * p.scale_log2;
+      q0[3] = Ops::hi(a.y) * p.scale_log2;
+      q1[0] = Ops::lo(bq.x) * p.scale_log2;
+      q1[1] = Ops::hi(bq.x) * p.scale_log2;
+      q1[2] = Ops::lo(bq.y) * p.scale_log2;
+      q1[3] = Ops::hi(bq.y) * p.scale_log2;
     }
     const int idx = lane >> (5 - kLog2N);         // logit index this lane ends up holding
     const int my_t = idx % kT;
@@ -239,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
 #pragma unroll
       for (int t = 0; t < kT; ++t) {
         const uint2 kr = lds64(kaddr + t * kRowBytes);
-        const float k0 = bf16lo_to_f32(kr.x), k1 = bf16hi_to_f32(kr.x);
-        const float k2 = bf16lo_to_f32(kr.y), k3 = bf16hi_to_f32(kr.y);
+        const float k0 = Ops::lo(kr.x), k1 = Ops::hi(kr.x);
+        const float k2 = Ops::lo(kr.y), k3 = Ops::hi(kr.y);
         part[t] = fmaf(q0[0], k0, fmaf(q0[1], k1, fmaf(q0[2], k2, q0[3] * k3)));
         part[kT + t] = fmaf(q1[0], k0, fmaf(q1[1], k1, fmaf(q1[2], k2, q1[3] * k3)));
       }
@@ -273,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w0) : "r"(wp_addr + 4 * t));
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w1) : "r"(wp_addr + 4 * (kT + t)));
           const uint2 vr = lds64(vaddr + t * kRowBytes);
-          const float v0 = bf16lo_to_f32(vr.x), v1 = bf16hi_to_f32(vr.x);
-          const float v2 = bf16lo_to_f32(vr.y), v3 = bf16hi_to_f32(vr.y);
+          const float v0 = Ops::lo(vr.x), v1 = Ops::hi(vr.x);
+          const float v2 = Ops::lo(vr.y), v3 = Ops::hi(vr.y);
           o0[0] = fmaf(w0, v0, o0[0]);
           o0[1] = fmaf(w0, v1, o0[1]);
           o0[2] = fmaf(w0, v2, o0[2]);
@@ -296,13 +299,13 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
     const float l1 = __shfl_sync(0xffffffffu, l, 16);
     if (nchunks == 1) {
       const float r0 = l0 > 0.f ? 1.f / l0 : 0.f, r1 = l1 > 0.f ? 1.f / l1 : 0.f;
-      __nv_bfloat16* orow = p.out + static_cast<int64_t>(b) * kHq * kHeadDim;
+      uint16_t* orow = p.out + static_cast<int64_t>(b) * kHq * kHeadDim;
       uint2 w;
-      w.x = pack_bf16x2(o0[0] * r0, o0[1] * r0);
-      w.y = pack_bf16x2(o0[2] * r0, o0[3] * r0);
+      w.x = Ops::pack(o0[0] * r0, o0[1] * r0);
+      w.y = Ops::pack(o0[2] * r0, o0[3] * r0);
       *reinterpret_cast<uint2*>(orow + (kGroup * h) * kHeadDim + lane * 4) = w;
-      w.x = pack_bf16x2(o1[0] * r1, o1[1] * r1);
-      w.y = pack_bf16x2(o1[2] * r1, o1[3] * r1);
+      w.x = Ops::pack(o1[0] * r1, o1[1] * r1);
+      w.y = Ops::pack(o1[2] * r1, o1[3] * r1);
       *reinterpret_cast<uint2*>(orow + (kGroup * h + 1) * kHeadDim + lane * 4) = w;
     } else {
       const int64_t slot = (static_cast<int64_t>(b) * p.nsplit + c) * kHq + kGroup * h;
@@ -354,10 +357,10 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
     }
     const float r = den > 0.f ? 1.f / den : 0.f;
     uint4 w;
-    w.x = pack_bf16x2(acc[0] * r, acc[1] * r);
-    w.y = pack_bf16x2(acc[2] * r, acc[3] * r);
-    w.z = pack_bf16x2(acc[4] * r, acc[5] * r);
-    w.w = pack_bf16x2(acc[6] * r, acc[7] * r);
+    w.x = Ops::pack(acc[0] * r, acc[1] * r);
+    w.y = Ops::pack(acc[2] * r, acc[3] * r);
+    w.z = Ops::pack(acc[4] * r, acc[5] * r);
+    w.w = Ops::pack(acc[6] * r, acc[7] * r);
     *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + hq) * kHeadDim + d0) = w;
   }
   if (threadIdx.x == 0) p.tickets[b] = 0;  // ready for the next call
@@ -372,6 +375,23 @@ constexpr size_t decode_smem_bytes() {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <Elem E>
+cudaError_t launch_typed(const DecodeParams& p, int32_t num_seqs, cudaStream_t stream) {
+  auto kernel = decode_split_kernel<E, kDecT, kDecStages>;
+  const size_t smem = decode_smem_bytes();
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  const dim3 grid(p.nsplit, num_seqs);
+  kernel<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
@@ -388,7 +408,7 @@ cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cac
                           int32_t num_blocks, const int32_t* block_tables, int32_t bt_stride,
                           const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float scale,
                           void* out, void* workspace, unsigned int* err, cudaStream_t stream,
-                          const FusedStore* fused) {
+                          const FusedStore* fused, Elem elem) {
   if (num_seqs == 0) return cudaSuccess;
   DecodeParams p;
   p.k_new = fused ? static_cast<const uint4*>(fused->k) : nullptr;
@@ -398,7 +418,7 @@ cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cac
   p.slot_mapping = fused ? fused->slot_mapping : nullptr;
   p.k_cache_w = static_cast<uint4*>(const_cast<void*>(k_cache));
   p.v_cache_w = static_cast<uint4*>(const_cast<void*>(v_cache));
-  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.q = static_cast<const uint16_t*>(q);
   p.q_row_stride = q_row_stride;
   p.k_cache = static_cast<const uint8_t*>(k_cache);
   p.v_cache = static_cast<const uint8_t*>(v_cache);
@@ -409,7 +429,7 @@ cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cac
   p.max_ctx = max_context_len;
   p.nsplit = decode_num_splits(max_context_len);
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = static_cast<uint16_t*>(out);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t ns = static_cast<size_t>(num_seqs);
   p.tickets = reinterpret_cast<int32_t*>(ws);
@@ -419,19 +439,8 @@ cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cac
   p.opart = reinterpret_cast<float*>(ws);
   p.err = err;
   if (p.nsplit == 0) p.nsplit = 1;
-  const size_t smem = decode_smem_bytes();
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<kDecT, kDecStages>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
-  const dim3 grid(p.nsplit, num_seqs);
-  decode_split_kernel<kDecT, kDecStages><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return elem == Elem::kF16 ? launch_typed<Elem::kF16>(p, num_seqs, stream)
+                            : launch_typed<Elem::kBF16>(p, num_seqs, stream);
 }
 
 }  // namespace pkv

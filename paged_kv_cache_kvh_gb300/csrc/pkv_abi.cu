@@ -24,13 +24,13 @@ cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cac
                           int32_t num_blocks, const int32_t* block_tables, int32_t bt_stride,
                           const int32_t* context_lens, int32_t num_seqs, int32_t max_context_len, float scale,
                           void* out, void* workspace, unsigned int* err, cudaStream_t stream,
-                          const FusedStore* fused = nullptr);
+                          const FusedStore* fused, Elem elem);
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len);
 cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
                            int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
                            int32_t num_blocks, const int32_t* cu_q, const int32_t* cu_k, int32_t max_seqlen_q,
                            int32_t max_seqlen_k, const int32_t* block_tables, int32_t bt_stride, int32_t num_seqs,
-                           float scale, void* out, unsigned int* err, cudaStream_t stream);
+                           float scale, void* out, unsigned int* err, cudaStream_t stream, Elem elem);
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
 cudaError_t launch_prefill_metadata(const int32_t* num_cached, const int32_t* num_scheduled,
                                     const int32_t* block_tables, int32_t bt_stride, int32_t num_blocks,
@@ -141,13 +141,22 @@ size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32
   return pkv::prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads);
 }
 
-int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
-                       int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
-                       int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                       int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_tables,
-                       int32_t block_table_stride, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
-                       int32_t head_dim, int32_t block_size, float softmax_scale, void* out, void* workspace,
-                       size_t workspace_bytes, cudaStream_t stream) {
+size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len) {
+  (void)num_heads;
+  if (num_seqs <= 0 || max_context_len <= 0) return 0;
+  return pkv::decode_workspace_bytes(num_seqs, max_context_len);
+}
+
+}  // extern "C"
+
+namespace {
+int prefill_common(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                   int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                   int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t max_seqlen_q,
+                   int32_t max_seqlen_k, const int32_t* block_tables, int32_t block_table_stride, int32_t num_seqs,
+                   int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   float softmax_scale, void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                   pkv::Elem elem) {
   int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || num_blocks < 0 ||
@@ -177,23 +186,15 @@ int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, con
   if (st != PKV_OK) return st;
   return launched(pkv::launch_prefill(q, q_row_stride, total_q, k, v, kv_row_stride, total_k, k_cache, v_cache,
                                       num_blocks, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                                      block_tables, block_table_stride, num_seqs, softmax_scale, out, err, stream));
+                                      block_tables, block_table_stride, num_seqs, softmax_scale, out, err, stream,
+                                      elem));
 }
 
-size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len) {
-  (void)num_heads;
-  if (num_seqs <= 0 || max_context_len <= 0) return 0;
-  return pkv::decode_workspace_bytes(num_seqs, max_context_len);
-}
-
-}  // extern "C"
-
-namespace {
 int decode_common(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
                   const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
                   int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                   int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream, const pkv::FusedStore* fused) {
+                  cudaStream_t stream, const pkv::FusedStore* fused, pkv::Elem elem) {
   int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_seqs > 65535 || num_blocks < 0 || block_table_stride < 0 || max_context_len < 0 ||
@@ -215,28 +216,15 @@ int decode_common(const void* q, int64_t q_row_stride, const void* k_cache, cons
   if (st != PKV_OK) return st;
   return launched(pkv::launch_decode(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables,
                                      block_table_stride, context_lens, num_seqs, max_context_len, softmax_scale,
-                                     out, workspace, err, stream, fused));
-}
-}  // namespace
-
-extern "C" {
-
-int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
-               const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
-               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-               int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
-               cudaStream_t stream) {
-  return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
-                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                       softmax_scale, out, workspace, workspace_bytes, stream, nullptr);
+                                     out, workspace, err, stream, fused, elem));
 }
 
-int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
-                     int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
-                     int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
-                     const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
-                     int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
-                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+int store_decode_common(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                        int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                        int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale,
+                        void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream, pkv::Elem elem) {
   if (num_seqs > 0) {
     if (!k || !v || !slot_mapping) return PKV_ERR_NULL_POINTER;
     const int64_t row = static_cast<int64_t>(num_kv_heads) * head_dim;
@@ -247,7 +235,82 @@ int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t
   const pkv::FusedStore fused{k, k_row_stride, v, v_row_stride, slot_mapping};
   return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
                        context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                       softmax_scale, out, workspace, workspace_bytes, stream, &fused);
+                       softmax_scale, out, workspace, workspace_bytes, stream, &fused, elem);
+}
+}  // namespace
+
+extern "C" {
+
+// The bf16 and fp16 entry points share one body each; only the element type differs.
+
+int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                       int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                       int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                       int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_tables,
+                       int32_t block_table_stride, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, float softmax_scale, void* out, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  return prefill_common(q, q_row_stride, total_q, k, v, kv_row_stride, total_k, k_cache, v_cache, num_blocks,
+                        cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_tables, block_table_stride,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, softmax_scale, out, workspace,
+                        workspace_bytes, stream, pkv::Elem::kBF16);
+}
+
+int pkv_prefill_varlen_f16(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
+                           int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
+                           int32_t num_blocks, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                           int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* block_tables,
+                           int32_t block_table_stride, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, float softmax_scale, void* out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  return prefill_common(q, q_row_stride, total_q, k, v, kv_row_stride, total_k, k_cache, v_cache, num_blocks,
+                        cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, block_tables, block_table_stride,
+                        num_seqs, num_heads, num_kv_heads, head_dim, block_size, softmax_scale, out, workspace,
+                        workspace_bytes, stream, pkv::Elem::kF16);
+}
+
+int pkv_decode(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,
+               const int32_t* block_tables, int32_t block_table_stride, const int32_t* context_lens,
+               int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+               int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
+  return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                       softmax_scale, out, workspace, workspace_bytes, stream, nullptr, pkv::Elem::kBF16);
+}
+
+int pkv_decode_f16(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                   int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                   const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                   int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
+                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return decode_common(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                       softmax_scale, out, workspace, workspace_bytes, stream, nullptr, pkv::Elem::kF16);
+}
+
+int pkv_store_decode(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                     int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                     int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                     const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale, void* out,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return store_decode_common(q, q_row_stride, k, k_row_stride, v, v_row_stride, slot_mapping, k_cache, v_cache,
+                             num_blocks, block_tables, block_table_stride, context_lens, num_seqs, num_heads,
+                             num_kv_heads, head_dim, block_size, max_context_len, softmax_scale, out, workspace,
+                             workspace_bytes, stream, pkv::Elem::kBF16);
+}
+
+int pkv_store_decode_f16(const void* q, int64_t q_row_stride, const void* k, int64_t k_row_stride, const void* v,
+                         int64_t v_row_stride, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                         int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale,
+                         void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return store_decode_common(q, q_row_stride, k, k_row_stride, v, v_row_stride, slot_mapping, k_cache, v_cache,
+                             num_blocks, block_tables, block_table_stride, context_lens, num_seqs, num_heads,
+                             num_kv_heads, head_dim, block_size, max_context_len, softmax_scale, out, workspace,
+                             workspace_bytes, stream, pkv::Elem::kF16);
 }
 
 int pkv_build_prefill_metadata(const int32_t* num_cached_tokens, const int32_t* num_scheduled_tokens,

@@ -9,6 +9,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "../../include/pkv.h"
@@ -207,11 +208,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr, uint32_t
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor, kind::f16 with fp32 D. ab_format is the A and B
+// element format (both the same): 0 = fp16, 1 = bf16.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                         uint32_t ab_format) {
   return (1u << 4)                           // D format: f32
-         | (1u << 7)                         // A format: bf16
-         | (1u << 10)                        // B format: bf16
+         | (ab_format << 7)                  // A format
+         | (ab_format << 10)                 // B format
          | ((a_mn_major ? 1u : 0u) << 15)    // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)    // B major-ness
          | ((static_cast<uint32_t>(N) >> 3) << 17)
@@ -234,5 +237,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+// ---- element types ----------------------------------------------------------
+//
+// q, k, v, the caches and the outputs hold one 16-bit type per call: bf16 (the
+// default) or IEEE fp16. Arithmetic is fp32 either way; the type only changes
+// how a packed pair of elements is widened and how results are rounded.
+
+enum class Elem : int { kBF16 = 0, kF16 = 1 };
+
+template <Elem E>
+struct ElemOps;
+
+template <>
+struct ElemOps<Elem::kBF16> {
+  static constexpr uint32_t kMmaFormat = 1;  // tcgen05 kind::f16 operand format code
+  __device__ static __forceinline__ float lo(uint32_t packed) { return bf16lo_to_f32(packed); }
+  __device__ static __forceinline__ float hi(uint32_t packed) { return bf16hi_to_f32(packed); }
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) { return pack_bf16x2(lo, hi); }
+};
+
+template <>
+struct ElemOps<Elem::kF16> {
+  static constexpr uint32_t kMmaFormat = 0;
+  __device__ static __forceinline__ float lo(uint32_t packed) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(packed & 0xFFFFu)));
+  }
+  __device__ static __forceinline__ float hi(uint32_t packed) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(packed >> 16)));
+  }
+  __device__ static __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+};
 
 }  // namespace pkv

@@ -28,6 +28,9 @@
 // grows by more than 8 (2^8 headroom in fp32/bf16), so O is rescaled rarely.
 // The last V tile's rows beyond the sequence are zeroed in shared memory
 // before use, so stale or NaN cache contents never reach the product.
+// The element type (bf16 or fp16) is a template parameter: it sets the
+// tensor-core operand format, the tensor maps' element type and how P and
+// the output are rounded; P <= 2^8 fits either type.
 #include <cuda.h>
 
 #include "pkv_common.cuh"
@@ -77,7 +80,7 @@ struct PrefillParams {
   int32_t total_k;  // rows of contiguous k/v (ignored when paged)
   int32_t paged;
   float scale_log2;
-  __nv_bfloat16* out;
+  uint16_t* out;  // 16-bit elements of the call's type
   unsigned int* err;
 };
 
@@ -103,9 +106,11 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+template <Elem E>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using Ops = ElemOps<E>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzle atoms.
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -226,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // =========================== MMA issuer ===========================
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, kHeadDim, false, true);
+      constexpr uint32_t idesc_s = idesc_f16kind_f32(kBM, kBN, false, false, Ops::kMmaFormat);
+      constexpr uint32_t idesc_pv = idesc_f16kind_f32(kBM, kHeadDim, false, true, Ops::kMmaFormat);
       bool ok = wait_or_abort(bar(kBarQ), 0, s_abort, p.err);
       auto slot_of = [](int i) { return i % kKvSlots; };
       auto par_of = [](int i) { return static_cast<uint32_t>((i / kKvSlots) & 1); };
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mx > m + 8.0f) m_use = mx;  // move the max only when it grows by > 2^8
       const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_use);
       l *= alpha;
-      // P = 2^(s*sl2 - m_use) as bf16 into the swizzled K-major A tile
+      // P = 2^(s*sl2 - m_use), rounded to the element type, into the swizzled K-major A tile
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         float e[8];
@@ -366,8 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int half = c >> 3;
         const uint32_t addr = prow + half * kHalfBytes + (((c & 7) ^ swz) << 4);
-        sts128(addr, pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
-               pack_bf16x2(e[6], e[7]));
+        sts128(addr, Ops::pack(e[0], e[1]), Ops::pack(e[2], e[3]), Ops::pack(e[4], e[5]), Ops::pack(e[6], e[7]));
       }
       m = m_use;
       // rescale the running output (PV_g(n-1) is complete: S_g(n) was issued after it)
@@ -394,8 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool row_ok = row < rows_valid;
-      __nv_bfloat16* orow =
-          p.out + (static_cast<int64_t>(cq0 + r0 + row) * kHq + (kGroup * hk + g)) * kHeadDim;
+      uint16_t* orow = p.out + (static_cast<int64_t>(cq0 + r0 + row) * kHq + (kGroup * hk + g)) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -406,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[j + 0]) * inv, __uint_as_float(r[j + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
+            w.x = Ops::pack(__uint_as_float(r[j + 0]) * inv, __uint_as_float(r[j + 1]) * inv);
+            w.y = Ops::pack(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
+            w.z = Ops::pack(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
+            w.w = Ops::pack(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
             *reinterpret_cast<uint4*>(orow + c * 32 + j) = w;
           }
         }
@@ -442,8 +445,10 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [rows, heads, 128] bf16 view with rows row_stride_elems apart; box = 128 rows x 1 head x 64 dims.
-bool encode_rows_heads_dims(CUtensorMap* tm, const void* base, int64_t rows, int heads, int64_t row_stride_elems) {
+// [rows, heads, 128] view of 16-bit elements with rows row_stride_elems apart;
+// box = 128 rows x 1 head x 64 dims.
+bool encode_rows_heads_dims(CUtensorMap* tm, const void* base, int64_t rows, int heads, int64_t row_stride_elems,
+                            Elem elem) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(heads),
@@ -452,9 +457,26 @@ bool encode_rows_heads_dims(CUtensorMap* tm, const void* base, int64_t rows, int
                                  static_cast<cuuint64_t>(row_stride_elems * 2)};
   const cuuint32_t box[3] = {64, 1, 128};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt = elem == Elem::kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(tm, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <Elem E>
+cudaError_t launch_typed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                         unsigned nblocks, cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = true;
+  }
+  prefill_tc_kernel<E><<<nblocks, kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -465,20 +487,20 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
                            int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
                            int32_t num_blocks, const int32_t* cu_q, const int32_t* cu_k, int32_t max_seqlen_q,
                            int32_t max_seqlen_k, const int32_t* block_tables, int32_t bt_stride, int32_t num_seqs,
-                           float scale, void* out, unsigned int* err, cudaStream_t stream) {
+                           float scale, void* out, unsigned int* err, cudaStream_t stream, Elem elem) {
   if (num_seqs == 0 || max_seqlen_q == 0 || total_q == 0) return cudaSuccess;
   CUtensorMap tq, tk, tv;
   const bool paged = block_tables != nullptr;
-  if (!encode_rows_heads_dims(&tq, q, total_q, kHq, q_row_stride)) return cudaErrorInvalidValue;
+  if (!encode_rows_heads_dims(&tq, q, total_q, kHq, q_row_stride, elem)) return cudaErrorInvalidValue;
   if (paged) {
     const int64_t slots = static_cast<int64_t>(num_blocks) * kBlockSize;
-    if (!encode_rows_heads_dims(&tk, k_cache, slots, kHkv, kHkv * kHeadDim) ||
-        !encode_rows_heads_dims(&tv, v_cache, slots, kHkv, kHkv * kHeadDim))
+    if (!encode_rows_heads_dims(&tk, k_cache, slots, kHkv, kHkv * kHeadDim, elem) ||
+        !encode_rows_heads_dims(&tv, v_cache, slots, kHkv, kHkv * kHeadDim, elem))
       return cudaErrorInvalidValue;
   } else {
     if (total_k == 0) return cudaErrorInvalidValue;
-    if (!encode_rows_heads_dims(&tk, k, total_k, kHkv, kv_row_stride) ||
-        !encode_rows_heads_dims(&tv, v, total_k, kHkv, kv_row_stride))
+    if (!encode_rows_heads_dims(&tk, k, total_k, kHkv, kv_row_stride, elem) ||
+        !encode_rows_heads_dims(&tv, v, total_k, kHkv, kv_row_stride, elem))
       return cudaErrorInvalidValue;
   }
   PrefillParams p;
@@ -495,21 +517,13 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
   p.total_k = paged ? 0 : total_k;
   p.paged = paged ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out = static_cast<uint16_t*>(out);
   p.err = err;
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
   const int64_t nblocks = static_cast<int64_t>(p.max_q_tiles) * num_seqs * kHkv;
   if (nblocks > 0x7fffffff) return cudaErrorInvalidValue;
-  prefill_tc_kernel<<<static_cast<unsigned>(nblocks), kThreads, kSmemBytes, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  const unsigned nb = static_cast<unsigned>(nblocks);
+  return elem == Elem::kF16 ? launch_typed<Elem::kF16>(tq, tk, tv, p, nb, stream)
+                            : launch_typed<Elem::kBF16>(tq, tk, tv, p, nb, stream);
 }
 
 }  // namespace pkv

@@ -13,12 +13,15 @@ import torch
 import oracle
 import workloads as W
 
-TOL_MAX = 2e-2    # max abs error on bf16 attention outputs (against the fp64 oracle)
+TOL_MAX = 2e-2    # max abs error on bf16 / fp16 attention outputs (against the fp64 oracle)
 TOL_MEAN = 2e-3   # mean abs error
+
+# torch element type -> the oracle's name for it
+ORACLE_DTYPE = {torch.bfloat16: "bf16", torch.float16: "f16"}
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """bf16 tensor (any device) -> host uint16 bit patterns."""
+    """16-bit tensor (any device) -> host uint16 bit patterns."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
@@ -52,9 +55,9 @@ class HostPool:
         return self.k.reshape(-1, *self.k.shape[2:]), self.v.reshape(-1, *self.v.shape[2:])
 
 
-def pool_tensors(num_blocks: int, gen, device):
+def pool_tensors(num_blocks: int, gen, device, dtype=torch.bfloat16):
     shape = (num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
-    return W.normal_bf16(shape, gen, device), W.normal_bf16(shape, gen, device)
+    return W.normal(shape, gen, device, dtype), W.normal(shape, gen, device, dtype)
 
 
 def poison_dead_slots(k_cache: torch.Tensor, v_cache: torch.Tensor, seqs, live_tokens):
@@ -70,7 +73,7 @@ def poison_dead_slots(k_cache: torch.Tensor, v_cache: torch.Tensor, seqs, live_t
             if cnt > 0:
                 live[int(blk), :cnt] = True
     dead = (~live).to(k_cache.device)
-    nan = torch.tensor(float("nan"), dtype=torch.bfloat16, device=k_cache.device)
+    nan = torch.tensor(float("nan"), dtype=k_cache.dtype, device=k_cache.device)
     k_cache[dead] = nan
     v_cache[dead] = nan
 

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import HostPool, assert_close, bits, poison_dead_slots, pool_tensors, to_dev
+from gpu_helpers import ORACLE_DTYPE, HostPool, assert_close, bits, poison_dead_slots, pool_tensors, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -20,18 +20,18 @@ def pkv():
 
 
 def _decode_step(pkv, wl, device, *, sample=None, poison=False, max_ctx=W.MAX_MODEL_LEN, fused=True,
-                 table_pad=0, stale_fill=None):
+                 table_pad=0, stale_fill=None, dtype=torch.bfloat16):
     """Store the new token of every sequence, then decode; check against the oracle."""
     gen = W.make_generator(wl.seed, device)
-    kc, vc = pool_tensors(wl.num_blocks, gen, device)
+    kc, vc = pool_tensors(wl.num_blocks, gen, device, dtype)
     seqs = wl.seqs
     B = len(seqs)
     if fused:
-        _, q, k, v = W.fused_qkv(B, gen, device)
+        _, q, k, v = W.fused_qkv(B, gen, device, dtype=dtype)
     else:
-        q = W.normal_bf16((B, W.HQ, W.HEAD_DIM), gen, device)
-        k = W.normal_bf16((B, W.HKV, W.HEAD_DIM), gen, device)
-        v = W.normal_bf16((B, W.HKV, W.HEAD_DIM), gen, device)
+        q = W.normal((B, W.HQ, W.HEAD_DIM), gen, device, dtype)
+        k = W.normal((B, W.HKV, W.HEAD_DIM), gen, device, dtype)
+        v = W.normal((B, W.HKV, W.HEAD_DIM), gen, device, dtype)
     if poison:
         poison_dead_slots(kc, vc, seqs, lambda s: s.num_tokens)
     width = max(len(s.block_table) for s in seqs) + table_pad
@@ -52,9 +52,11 @@ def _decode_step(pkv, wl, device, *, sample=None, poison=False, max_ctx=W.MAX_MO
     btd = to_dev(bt, device)
     ws = pkv.decode_workspace(B, max_ctx, device)
     pkv.pkv_store_kvcache(k, v, kc, vc, slot)
-    out = pkv.pkv_decode(q, kc, vc, btd, ctx, max_ctx, W.SCALE, ws)
+    decode = pkv.pkv_decode_f16 if dtype == torch.float16 else pkv.pkv_decode
+    out = decode(q, kc, vc, btd, ctx, max_ctx, W.SCALE, ws)
     torch.cuda.synchronize()
     assert pkv.pkv_device_error() == 0
+    assert out.dtype == dtype
 
     # oracle: its own store into its own copy, then its own decode
     om = oracle.prepare_decode(host.seqs, W.BLOCK_SIZE)
@@ -62,7 +64,7 @@ def _decode_step(pkv, wl, device, *, sample=None, poison=False, max_ctx=W.MAX_MO
     orc = oracle.default()
     orc.store_kvcache(kb[sample], vb[sample], ks, vs, om["slot_mapping"])
     ref = orc.decode(qb[sample], host.k, host.v, om["block_tables"], om["context_lens"], W.SCALE,
-                     num_kv_heads=W.HKV)
+                     num_kv_heads=W.HKV, dtype=ORACLE_DTYPE[dtype])
     got = out[torch.tensor(sample, device=device)]
     assert_close(got, ref, wl.name)
     return out, (kc, vc, k, v, q, slot, ctx, btd, ws)
@@ -178,16 +180,19 @@ def test_bad_block_and_slot_are_flagged_not_dereferenced(pkv):
     assert torch.all(torch.isfinite(out.float())) and pkv.pkv_device_error() == 0
 
 
-@pytest.mark.parametrize("factory", [W.tiny_decode, W.batched_decode, lambda: W.sweep_decode(num_layers=1)])
-def test_store_decode_fused_matches_separate(pkv, factory):
+@pytest.mark.parametrize("factory,dtype", [(W.tiny_decode, torch.bfloat16), (W.batched_decode, torch.bfloat16),
+                                           (lambda: W.sweep_decode(num_layers=1), torch.bfloat16),
+                                           (W.tiny_decode, torch.float16), (W.batched_decode, torch.float16)])
+def test_store_decode_fused_matches_separate(pkv, factory, dtype):
     """pkv_store_decode == pkv_store_kvcache then pkv_decode: same output and
-    the same cache, bit for bit (padding rows included)."""
+    the same cache, bit for bit (padding rows included); likewise for the
+    fp16 entry points."""
     dev = "cuda"
     wl = factory()
     gen = W.make_generator(wl.seed + 1000, dev)
-    kc, vc = pool_tensors(wl.num_blocks, gen, dev)
+    kc, vc = pool_tensors(wl.num_blocks, gen, dev, dtype)
     B, pad = len(wl.seqs), 3
-    _, q, k, v = W.fused_qkv(B + pad, gen, dev)
+    _, q, k, v = W.fused_qkv(B + pad, gen, dev, dtype=dtype)
     meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE, table_width=16)
     slot = torch.full((B + pad,), -1, dtype=torch.int32, device=dev)
     slot[:B] = to_dev(meta["slot_mapping"], dev)
@@ -197,9 +202,12 @@ def test_store_decode_fused_matches_separate(pkv, factory):
     bt[:B] = to_dev(meta["block_tables"], dev)
     kc2, vc2 = kc.clone(), vc.clone()
     ws = pkv.decode_workspace(B + pad, W.MAX_MODEL_LEN, dev)
+    f16 = dtype == torch.float16
+    decode = pkv.pkv_decode_f16 if f16 else pkv.pkv_decode
+    store_decode = pkv.pkv_store_decode_f16 if f16 else pkv.pkv_store_decode
     pkv.pkv_store_kvcache(k, v, kc, vc, slot)
-    ref = pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
-    got = pkv.pkv_store_decode(q, k, v, slot, kc2, vc2, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+    ref = decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+    got = store_decode(q, k, v, slot, kc2, vc2, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
     torch.cuda.synchronize()
     assert pkv.pkv_device_error() == 0
     assert torch.equal(got, ref)
@@ -224,3 +232,51 @@ def test_store_decode_rejects_foreign_slot(pkv):
     assert pkv.pkv_device_error() & pkv.PKV_DEVERR_BAD_SLOT
     bad = int(meta["slot_mapping"][1]) - 1
     assert torch.equal(kc.view(-1, 8, 128)[bad], before.view(-1, 8, 128)[bad])
+
+
+# ---- fp16 element type (pkv_decode_f16) ------------------------------------
+
+def test_f16_tiny_decode_poisoned_and_stale_tables(pkv):
+    _decode_step(pkv, W.tiny_decode(seed=12), "cuda", poison=True, table_pad=3, stale_fill=123456,
+                 dtype=torch.float16)
+
+
+def test_f16_ragged_contexts(pkv):
+    ctxs = [1, 2, 255, 256, 257, 511, 512, 513, 1000, 4096]
+    rng = np.random.default_rng(40)
+    nb = sum(W.blocks_for(c) for c in ctxs) + 5
+    wl = W.Workload("ragged_f16", 78, W._decode_seqs(ctxs, nb, rng), nb, "decode")
+    _decode_step(pkv, wl, "cuda", poison=True, fused=False, dtype=torch.float16)
+
+
+def test_f16_batched_decode_full_size(pkv):
+    """256 sequences, context 512..4096, fp16: sampled sequences against the oracle."""
+    wl = W.batched_decode()
+    ctx = np.array([s.num_tokens for s in wl.seqs])
+    rng = np.random.default_rng(2)
+    sample = sorted({int(ctx.argmin()), int(ctx.argmax()), *rng.choice(len(ctx), 8, replace=False).tolist()})
+    _decode_step(pkv, wl, "cuda", sample=sample, dtype=torch.float16)
+
+
+def test_f16_and_bf16_see_the_same_values(pkv):
+    """Values exact in both types (small integers times powers of two): the
+    bf16 and fp16 kernels read the same numbers and must agree to within
+    one rounding of the output."""
+    dev = "cuda"
+    wl = W.tiny_decode(seed=13)
+    rng = np.random.default_rng(13)
+    shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+    kc32 = torch.from_numpy(rng.integers(-8, 9, size=shape) / 8.0).float()
+    vc32 = torch.from_numpy(rng.integers(-8, 9, size=shape) / 4.0).float()
+    q32 = torch.from_numpy(rng.integers(-8, 9, size=(4, W.HQ, W.HEAD_DIM)) / 8.0).float()
+    meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE)
+    bt, ctx = to_dev(meta["block_tables"], dev), to_dev(meta["context_lens"], dev)
+    ws = pkv.decode_workspace(4, W.MAX_MODEL_LEN, dev)
+    outs = {}
+    for dt, fn in ((torch.bfloat16, pkv.pkv_decode), (torch.float16, pkv.pkv_decode_f16)):
+        outs[dt] = fn(q32.to(dev, dt), kc32.to(dev, dt), vc32.to(dev, dt), bt, ctx, W.MAX_MODEL_LEN, W.SCALE,
+                      ws).float()
+    torch.cuda.synchronize()
+    diff = (outs[torch.bfloat16] - outs[torch.float16]).abs()
+    assert float(diff.max()) <= 2.0 ** -8 * 2.0 + 1e-6       # one bf16 ulp of |o| <= 2, plus fp16 rounding
+    assert pkv.pkv_device_error() == 0

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import HostPool, assert_close, bits, poison_dead_slots, pool_tensors, to_dev
+from gpu_helpers import ORACLE_DTYPE, HostPool, assert_close, bits, poison_dead_slots, pool_tensors, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -45,15 +45,16 @@ def _rows_sample(cu_q, rng, per_seq=6):
     return np.array(rows, dtype=np.int64)
 
 
-def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguous=False):
+def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguous=False, dtype=torch.bfloat16):
     """Store the scheduled tokens of every sequence, run paged prefill, compare
     with the oracle (all rows, or sampled rows) and optionally with the
     contiguous-keys mode of the same kernel."""
     dev = "cuda"
     gen = W.make_generator(seed, dev)
-    kc, vc = pool_tensors(nb, gen, dev)
+    kc, vc = pool_tensors(nb, gen, dev, dtype)
     T = sum(s.num_scheduled_tokens for s in seqs)
-    _, q, k, v = W.fused_qkv(T, gen, dev)
+    _, q, k, v = W.fused_qkv(T, gen, dev, dtype=dtype)
+    prefill = pkv.pkv_prefill_varlen_f16 if dtype == torch.float16 else pkv.pkv_prefill_varlen
     if poison:
         poison_dead_slots(kc, vc, seqs, lambda s: s.num_tokens)
     meta = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
@@ -69,10 +70,11 @@ def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguou
     cu_k = to_dev(meta["cu_seqlens_k"], dev)
     bt = to_dev(meta["block_tables"], dev)
     pkv.pkv_store_kvcache(k, v, kc, vc, slot)
-    out = pkv.pkv_prefill_varlen(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE,
-                                 k_cache=kc, v_cache=vc, block_tables=bt)
+    out = prefill(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE,
+                  k_cache=kc, v_cache=vc, block_tables=bt)
     torch.cuda.synchronize()
     assert pkv.pkv_device_error() == 0
+    assert out.dtype == dtype
 
     om = oracle.prepare_prefill(host.seqs, W.BLOCK_SIZE)
     ks, vs = host.slots()
@@ -80,7 +82,7 @@ def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguou
     orc.store_kvcache(kb, vb, ks, vs, om["slot_mapping"])
     bt_o = oracle.pad_block_tables(host.seqs)
     ref = orc.prefill_varlen(qb, om["cu_seqlens_q"], om["cu_seqlens_k"], W.SCALE, k_cache=host.k, v_cache=host.v,
-                             block_tables=bt_o, num_kv_heads=W.HKV, rows=sample_rows)
+                             block_tables=bt_o, num_kv_heads=W.HKV, rows=sample_rows, dtype=ORACLE_DTYPE[dtype])
     if sample_rows is None:
         assert_close(out, ref, "prefill")
     else:
@@ -88,7 +90,7 @@ def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguou
         assert_close(got, ref, "prefill (sampled rows)")
     if check_contiguous:
         # no prefix: the same keys from contiguous k/v must give the identical result
-        out2 = pkv.pkv_prefill_varlen(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k=k, v=v)
+        out2 = prefill(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k=k, v=v)
         torch.cuda.synchronize()
         assert torch.equal(out, out2)
     return out
@@ -165,10 +167,44 @@ def test_bad_seqlens_flagged(pkv):
 
 
 def test_many_items_per_cta_with_tail_tiles(pkv):
-    """Hundreds of short sequences: every CTA of the persistent kernel takes
-    many work items in a row, most ending in a partial (zeroed) V tile."""
+    """Hundreds of short sequences (thousands of query tiles, most of them
+    ending in a partial, zeroed V tile), with and without cached prefixes."""
     rng = np.random.default_rng(99)
     specs = [(int(c), int(s)) for c, s in zip(rng.integers(0, 300, 400), rng.integers(1, 200, 400))]
     seqs, nb = _seqs_with_tables(specs, rng)
     cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in seqs])])
     _run(pkv, seqs, nb, seed=99, poison=True, sample_rows=_rows_sample(cu, np.random.default_rng(5), 3))
+
+
+# ---- fp16 element type (pkv_prefill_varlen_f16) ----------------------------
+
+@pytest.mark.parametrize("lens", [[1, 255, 256, 257, 300, 513], [1024, 77]])
+def test_f16_prefill_no_prefix(pkv, lens):
+    rng = np.random.default_rng(500 + sum(lens))
+    seqs, nb = _seqs_with_tables([(0, n) for n in lens], rng)
+    _run(pkv, seqs, nb, seed=500 + len(lens), poison=True, check_contiguous=True, dtype=torch.float16)
+
+
+@pytest.mark.parametrize("specs", [[(1, 1), (300, 129), (44, 300)], [(1024, 64), (1024, 512)], [(3000, 1000)]])
+def test_f16_prefill_with_cached_prefix(pkv, specs):
+    rng = np.random.default_rng(600 + len(specs))
+    seqs, nb = _seqs_with_tables(specs, rng)
+    _run(pkv, seqs, nb, seed=600 + sum(s for _, s in specs), poison=True, dtype=torch.float16)
+
+
+def test_f16_varlen_prefill_full_size_first_call(pkv):
+    """The first <=16384-token call of the 64-prompt workload, fp16, sampled rows."""
+    wl = W.varlen_prefill()
+    call = wl.seqs[0]
+    cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in call])])
+    _run(pkv, call, wl.num_blocks, seed=700, sample_rows=_rows_sample(cu, np.random.default_rng(7), 3),
+         check_contiguous=True, dtype=torch.float16)
+
+
+def test_f16_prefix_prefill_full_size(pkv):
+    """128 sequences sharing a 1024-token prefix, fp16, sampled rows."""
+    wl = W.prefix_prefill()
+    call = wl.seqs[0]
+    cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in call])])
+    _run(pkv, call, wl.num_blocks, seed=704, sample_rows=_rows_sample(cu, np.random.default_rng(8), 2),
+         dtype=torch.float16)

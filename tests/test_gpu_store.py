@@ -19,20 +19,21 @@ def pkv():
     return m
 
 
-@pytest.mark.parametrize("n_tokens,num_blocks,fused,hkv", [
-    (1, 1, True, 8), (4, 16, True, 8), (256, 64, True, 8), (16384, 160, True, 8), (1000, 8, False, 8),
-    (333, 4, False, 2), (77, 2, False, 3)])
-def test_store_bit_exact(pkv, n_tokens, num_blocks, fused, hkv):
+@pytest.mark.parametrize("n_tokens,num_blocks,fused,hkv,dtype", [
+    (1, 1, True, 8, torch.bfloat16), (4, 16, True, 8, torch.bfloat16), (256, 64, True, 8, torch.bfloat16),
+    (16384, 160, True, 8, torch.bfloat16), (1000, 8, False, 8, torch.bfloat16), (333, 4, False, 2, torch.bfloat16),
+    (77, 2, False, 3, torch.bfloat16), (512, 32, True, 8, torch.float16), (77, 2, False, 3, torch.float16)])
+def test_store_bit_exact(pkv, n_tokens, num_blocks, fused, hkv, dtype):
     dev = "cuda"
     gen = W.make_generator(n_tokens, dev)
     rng = np.random.default_rng(n_tokens)
-    kc = W.normal_bf16((num_blocks * W.BLOCK_SIZE, hkv, W.HEAD_DIM), gen, dev)
-    vc = W.normal_bf16((num_blocks * W.BLOCK_SIZE, hkv, W.HEAD_DIM), gen, dev)
+    kc = W.normal((num_blocks * W.BLOCK_SIZE, hkv, W.HEAD_DIM), gen, dev, dtype)
+    vc = W.normal((num_blocks * W.BLOCK_SIZE, hkv, W.HEAD_DIM), gen, dev, dtype)
     if fused:
-        _, _, k, v = W.fused_qkv(n_tokens, gen, dev, hkv=hkv)
+        _, _, k, v = W.fused_qkv(n_tokens, gen, dev, hkv=hkv, dtype=dtype)
     else:
-        k = W.normal_bf16((n_tokens, hkv, W.HEAD_DIM), gen, dev)
-        v = W.normal_bf16((n_tokens, hkv, W.HEAD_DIM), gen, dev)
+        k = W.normal((n_tokens, hkv, W.HEAD_DIM), gen, dev, dtype)
+        v = W.normal((n_tokens, hkv, W.HEAD_DIM), gen, dev, dtype)
     slots = rng.permutation(num_blocks * W.BLOCK_SIZE)[:n_tokens].astype(np.int32)
     slots[rng.random(n_tokens) < 0.1] = -1                      # padding tokens
     kc_h, vc_h, kb, vb = bits(kc), bits(vc), bits(k), bits(v)

@@ -8,8 +8,9 @@ and the CUDA path each derive those from what is generated here.
 Recipe (the same for every consumer):
 * integer draws (lengths, block permutations) use NumPy PCG64 seeded with the
   workload's seed;
-* bf16 tensors are fp32 N(0,1) from a seeded ``torch.Generator`` on the
-  target device, rounded to nearest-even bf16 (torch's conversion);
+* 16-bit tensors are fp32 N(0,1) from a seeded ``torch.Generator`` on the
+  target device, rounded to nearest-even bf16 (the default) or fp16 (torch's
+  conversions); the fp16 cases draw the same fp32 stream as the bf16 ones;
 * physical block ids are a seeded permutation of the pool, so consecutive
   logical blocks of a sequence land on scattered physical blocks;
 * every pool slot, used or not, starts as N(0,1) (tests may poison unused
@@ -53,20 +54,24 @@ def make_generator(seed: int, device) -> torch.Generator:
     return g
 
 
-def normal_bf16(shape, gen: torch.Generator, device, chunk_elems: int = 1 << 27) -> torch.Tensor:
-    """bf16 N(0,1) tensor, generated in fp32 chunks to bound temporary memory."""
-    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+def normal(shape, gen: torch.Generator, device, dtype=torch.bfloat16, chunk_elems: int = 1 << 27) -> torch.Tensor:
+    """N(0,1) tensor of a 16-bit type, generated in fp32 chunks to bound temporary memory."""
+    out = torch.empty(shape, dtype=dtype, device=device)
     flat = out.view(-1)
     for s in range(0, flat.numel(), chunk_elems):
         e = min(s + chunk_elems, flat.numel())
-        flat[s:e] = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+        flat[s:e] = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32).to(dtype)
     return out
 
 
-def fused_qkv(num_tokens: int, gen: torch.Generator, device, hq=HQ, hkv=HKV, d=HEAD_DIM):
+def normal_bf16(shape, gen: torch.Generator, device, chunk_elems: int = 1 << 27) -> torch.Tensor:
+    return normal(shape, gen, device, torch.bfloat16, chunk_elems)
+
+
+def fused_qkv(num_tokens: int, gen: torch.Generator, device, hq=HQ, hkv=HKV, d=HEAD_DIM, dtype=torch.bfloat16):
     """q, k, v as views of one fused projection output [N, (hq+2*hkv)*d], the
     layout nano-vLLM's attention receives (q/k/v rows strided by the fused width)."""
-    qkv = normal_bf16((num_tokens, (hq + 2 * hkv) * d), gen, device)
+    qkv = normal((num_tokens, (hq + 2 * hkv) * d), gen, device, dtype)
     q = qkv[:, : hq * d].view(num_tokens, hq, d)
     k = qkv[:, hq * d: (hq + hkv) * d].view(num_tokens, hkv, d)
     v = qkv[:, (hq + hkv) * d:].view(num_tokens, hkv, d)
