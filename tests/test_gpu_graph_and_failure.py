@@ -81,6 +81,69 @@ def test_layers_in_one_graph_match_eager_and_oracle(pkv):
     assert pkv.pkv_device_error() == 0
 
 
+def test_padded_graph_replay_matches_unpadded(pkv):
+    """A 200-sequence decode step replayed through a graph captured for 256
+    rows, with the buffer refresh the pages do before a replay
+    (slot_mapping.fill_(-1), context_lens.zero_(), then only the live part of
+    each buffer overwritten, so padding rows and table tails keep an earlier
+    step's contents). The live rows must equal an eager, unpadded store +
+    decode bit for bit, padding rows are zeros, and the caches end identical
+    (padding stores nothing)."""
+    dev = "cuda"
+    wl = W.padded_decode()
+    B, G = len(wl.seqs), wl.graph_batch
+    width = W.MAX_MODEL_LEN // W.BLOCK_SIZE
+    gen = W.make_generator(wl.seed, dev)
+    kc, vc = pool_tensors(wl.num_blocks, gen, dev)
+    _, q_new, k_new, v_new = W.fused_qkv(B, gen, dev)
+    meta = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE)
+    rng = np.random.default_rng(7)
+    # static graph buffers, first filled by an "earlier step" of 256 live rows
+    _, q_s, k_s, v_s = W.fused_qkv(G, gen, dev)
+    slot_s = to_dev(rng.permutation(wl.num_blocks * W.BLOCK_SIZE)[:G].astype(np.int32), dev)
+    ctx_s = to_dev(rng.integers(1, W.MAX_MODEL_LEN + 1, size=G).astype(np.int32), dev)
+    bt_s = to_dev(rng.integers(0, wl.num_blocks, size=(G, width)).astype(np.int32), dev)
+    out_s = torch.empty(G, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    ws = pkv.decode_workspace(G, W.MAX_MODEL_LEN, dev)
+    kc_eager, vc_eager = kc.clone(), vc.clone()
+    kc0, vc0 = kc.clone(), vc.clone()
+
+    def step():
+        pkv.pkv_store_kvcache(k_s, v_s, kc, vc, slot_s)
+        pkv.pkv_decode(q_s, kc, vc, bt_s, ctx_s, W.MAX_MODEL_LEN, W.SCALE, ws, out=out_s)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    torch.cuda.synchronize()
+    kc.copy_(kc0)
+    vc.copy_(vc0)
+    # the refresh before a replay, as the pages' run_model does it
+    slot_s.fill_(-1)
+    ctx_s.zero_()
+    w = meta["block_tables"].shape[1]
+    bt_s[:B, :w] = to_dev(meta["block_tables"], dev)
+    slot_s[:B] = to_dev(meta["slot_mapping"], dev)
+    ctx_s[:B] = to_dev(meta["context_lens"], dev)
+    q_s[:B], k_s[:B], v_s[:B] = q_new, k_new, v_new
+    g.replay()
+    # eager, unpadded
+    ws2 = pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev)
+    pkv.pkv_store_kvcache(k_new, v_new, kc_eager, vc_eager, to_dev(meta["slot_mapping"], dev))
+    ref = pkv.pkv_decode(q_new, kc_eager, vc_eager, to_dev(meta["block_tables"], dev),
+                         to_dev(meta["context_lens"], dev), W.MAX_MODEL_LEN, W.SCALE, ws2)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() == 0
+    assert torch.equal(out_s[:B], ref)
+    assert torch.all(out_s[B:] == 0)
+    assert torch.equal(kc, kc_eager) and torch.equal(vc, vc_eager)
+
+
 def test_bounded_wait_times_out_and_gpu_stays_usable(pkv):
     pkv.pkv_device_error(clear=True)
     pkv.pkv_selftest_wait_timeout(2_000_000)     # 2 ms on a barrier nobody completes

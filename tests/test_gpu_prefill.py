@@ -208,3 +208,70 @@ def test_f16_prefix_prefill_full_size(pkv):
     cu = np.concatenate([[0], np.cumsum([s.num_scheduled_tokens for s in call])])
     _run(pkv, call, wl.num_blocks, seed=704, sample_rows=_rows_sample(cu, np.random.default_rng(8), 2),
          dtype=torch.float16)
+
+
+# ---- chunked prefill: calls in order, the cache carried from call to call ----
+
+def _run_calls(pkv, calls, nb, seed, rng, *, per_seq=None, poison=False):
+    """Run a sequence of prefill calls (each: store its new tokens, then paged
+    prefill) on one pool, as consecutive scheduler steps do; the oracle keeps
+    its own copy of the pool and applies the same stores in the same order.
+    per_seq=None compares every row, else that many sampled rows per sequence."""
+    dev = "cuda"
+    gen = W.make_generator(seed, dev)
+    kc, vc = pool_tensors(nb, gen, dev)
+    if poison:   # slots past each prompt's end are never read
+        poison_dead_slots(kc, vc, [s for call in calls for s in call], lambda s: s.num_tokens)
+    host = HostPool(kc, vc, [s for call in calls for s in call])
+    ks, vs = host.slots()
+    orc = oracle.default()
+    for ci, call in enumerate(calls):
+        T = sum(s.num_scheduled_tokens for s in call)
+        _, q, k, v = W.fused_qkv(T, gen, dev)
+        qb, kb, vb = bits(q), bits(k), bits(v)
+        meta = pkv.metadata.prepare_prefill(call, W.BLOCK_SIZE, force_block_tables=True)
+        pkv.pkv_store_kvcache(k, v, kc, vc, to_dev(meta["slot_mapping"], dev))
+        out = pkv.pkv_prefill_varlen(q, to_dev(meta["cu_seqlens_q"], dev), to_dev(meta["cu_seqlens_k"], dev),
+                                     meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc,
+                                     block_tables=to_dev(meta["block_tables"], dev))
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_error() == 0
+        oseqs = [oracle.SeqState(s.num_tokens, [host.remap[int(x)] for x in s.block_table], s.num_cached_tokens,
+                                 s.num_scheduled_tokens) for s in call]
+        om = oracle.prepare_prefill(oseqs, W.BLOCK_SIZE)
+        assert np.array_equal(om["cu_seqlens_k"], meta["cu_seqlens_k"])
+        orc.store_kvcache(kb, vb, ks, vs, om["slot_mapping"])
+        rows = None if per_seq is None else _rows_sample(om["cu_seqlens_q"], rng, per_seq)
+        ref = orc.prefill_varlen(qb, om["cu_seqlens_q"], om["cu_seqlens_k"], W.SCALE, k_cache=host.k,
+                                 v_cache=host.v, block_tables=oracle.pad_block_tables(oseqs), num_kv_heads=W.HKV,
+                                 rows=rows)
+        if rows is None:
+            assert_close(out, ref, f"call {ci}")
+        else:
+            got = out[torch.from_numpy(rows[:, 0]).to(dev), torch.from_numpy(rows[:, 1]).to(dev)]
+            assert_close(got, ref, f"call {ci} (sampled rows)")
+
+
+def test_chunked_prefill_small_all_rows(pkv):
+    """Prompts of 700/300/900/1300 tokens under a 500-token budget: chunks
+    continue at positions 500, 1000 (mid-block), a tail shares its call with
+    a whole prompt; every row of every call against the oracle."""
+    lengths = [700, 300, 900, 1300]
+    plan = W.schedule_prefill_chunks(lengths, 500)
+    assert any(start % W.BLOCK_SIZE for call in plan for _, start, _ in call)
+    rng = np.random.default_rng(31)
+    nb = sum(W.blocks_for(n) for n in lengths) + 4
+    perm = rng.permutation(nb)
+    tables, cur = [], 0
+    for n in lengths:
+        tables.append([int(x) for x in perm[cur:cur + W.blocks_for(n)]])
+        cur += W.blocks_for(n)
+    calls = [[W.SeqSpec(lengths[i], tables[i], start, cnt) for i, start, cnt in call] for call in plan]
+    _run_calls(pkv, calls, nb, seed=31, rng=rng, poison=True)
+
+
+def test_chunked_prefill_full_size(pkv):
+    """16 prompts of 4096..12288 tokens under a 5000-token budget (35 calls,
+    19 chunks starting mid-block): every call in order, sampled rows."""
+    wl = W.chunked_prefill()
+    _run_calls(pkv, wl.seqs, wl.num_blocks, seed=wl.seed, rng=np.random.default_rng(6), per_seq=3)

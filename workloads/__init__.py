@@ -91,6 +91,7 @@ class Workload:
     head_dim: int = HEAD_DIM
     block_size: int = BLOCK_SIZE
     scale: float = SCALE
+    graph_batch: int = 0            # decode replayed through a graph of this many rows (0: eager)
     notes: str = ""
 
 
@@ -197,10 +198,81 @@ def prefix_prefill(seed: int = 4, num_seqs: int = 128, prefix_len: int = 1024, l
                     nb, "prefill")
 
 
+def schedule_prefill_chunks(lengths, budget: int):
+    """The prefill half of the scheduler in the newest listing ("vLLM 学习笔记 02：nano-vllm
+    源码逐段精读", engine/scheduler.py ``schedule``), without prefix-cache hits:
+    prompts wait in order; a call admits the prompt at the head of the queue
+    while token budget is left; a prompt that does not fit is cut only when it
+    is the first of its call (it gets what is left and stays at the head, its
+    computed tokens counting as cached next time); otherwise the call closes.
+
+    Returns a list of calls, each a list of (prompt index, start, count)."""
+    lengths = [int(n) for n in lengths]
+    done = [0] * len(lengths)
+    head, calls = 0, []
+    while head < len(lengths):
+        call, used = [], 0
+        while head < len(lengths) and used < budget:
+            need = lengths[head] - done[head]
+            left = budget - used
+            if left < need and call:
+                break
+            take = min(need, left)
+            call.append((head, done[head], take))
+            used += take
+            done[head] += take
+            if done[head] == lengths[head]:
+                head += 1
+        calls.append(call)
+    return calls
+
+
+def chunked_prefill(seed: int = 6, num_prompts: int = 16, lo: int = 4096, hi: int = 12288,
+                    budget: int = 5000) -> Workload:
+    """16 prompts of 4096..12288 tokens under a 5000-token budget: every
+    prompt longer than the budget is computed in chunks over several calls.
+    5000 is not a multiple of the 256-token block, so continued chunks start
+    in the middle of a block. Each
+    prompt's blocks are allocated for its whole length when it is first
+    admitted (engine/block_manager.py ``allocate``), from a shuffled pool."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lengths = rng.integers(lo, hi + 1, size=num_prompts)
+    need = sum(blocks_for(int(n)) for n in lengths)
+    nb = need + 64
+    perm = rng.permutation(nb)
+    tables, cursor = [], 0
+    for n in lengths:
+        t, cursor = _take_blocks(perm, cursor, blocks_for(int(n)))
+        tables.append(t)
+    calls = [[SeqSpec(num_tokens=int(lengths[i]), block_table=list(tables[i]), num_cached_tokens=start,
+                      num_scheduled_tokens=cnt) for i, start, cnt in call]
+             for call in schedule_prefill_chunks(lengths, budget)]
+    return Workload(f"chunked_prefill_{num_prompts}p_len{lo}-{hi}_budget{budget}", seed, calls, nb, "prefill",
+                    notes=f"token budget {budget}")
+
+
+def padded_decode(seed: int = 7, num_seqs: int = 200, graph_batch: int = 256, num_blocks: int = 8192,
+                  lo: int = 512, hi: int = 4096) -> Workload:
+    """A decode step replayed through a CUDA graph captured for a larger batch
+    (engine/model_runner.py ``run_model``: the graph for the next captured
+    size >= the batch is replayed after ``slot_mapping.fill_(-1)``,
+    ``context_lens.zero_()`` and an overwrite of only the live part of the
+    block-table buffer). 200 live sequences (context 512..4096) in a graph of
+    256 rows; rows 200..255 are padding, and table entries past a row's live
+    blocks keep whatever an earlier step left there."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    ctx = rng.integers(lo, hi + 1, size=num_seqs)
+    seqs = _decode_seqs(ctx, num_blocks, rng)
+    return Workload(f"padded_decode_b{num_seqs}_graph{graph_batch}", seed, seqs, num_blocks, "decode",
+                    graph_batch=graph_batch)
+
+
 CONFIGS = {
     1: tiny_decode,
     2: batched_decode,
     3: varlen_prefill,
     4: prefix_prefill,
     5: sweep_decode,
+    6: chunked_prefill,
+    7: padded_decode,
 }
