@@ -56,14 +56,19 @@ def _peaks():
 
 
 def _src_hash(name):
-    with open(os.path.join(ROOT, "paged_kv_cache_kvh_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of a kernel's source file plus the device header it includes."""
+    h = hashlib.sha256()
+    for part in (name, "pkv_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_kvh_gb300", "csrc", part), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def _traffic(kernel_file, units_now):
+def _traffic(kernel_file, units_now, case=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current source of the kernel (else None). Scaled by units processed
-    when the capture used a smaller case of the same kernel."""
+    when the capture used a smaller case of the same kernel; ``case`` picks a
+    capture taken on one specific workload (no scaling across workloads)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -72,6 +77,9 @@ def _traffic(kernel_file, units_now):
     e = d.get(kernel_file)
     if not e or e.get("src_sha") != _src_hash(kernel_file):
         return None
+    if case is not None:
+        c = e.get("cases", {}).get(case)
+        return None if c is None else c["dram_bytes_per_launch"]
     return e["dram_bytes_per_launch"] * (units_now / e["units"]) if e.get("units") else e["dram_bytes_per_launch"]
 
 
@@ -329,7 +337,8 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
                                   "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
                                   "peak_source": ("measured bf16 dense (cuBLAS burst) x nominal fp16/bf16 ratio 1"
                                                   if f16 else "measured bf16 dense (cuBLAS burst)"),
-                                  "traffic": None if f16 else _traffic("prefill.cu", flops)},
+                                  "traffic": None if f16 else _traffic("prefill.cu", flops, case=name),
+                                  "traffic_note": "ncu DRAM bytes of one launch (the workload's first call)"},
                      "store_ms": round(t_st, 4), "store_gbs": round(store_bytes / (t_st * 1e-3) / 1e9, 1),
                      "l2": "256 MB buffer written between launches"}
     assert pkv.pkv_device_error() == 0
