@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          mma_bf16_ss(tmem + g * 128, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+          mma_f16kind_ss(tmem + g * 128, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
                       idesc_s, ks > 0 ? 1u : 0u);
         }
       };
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
           const uint32_t aoff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          mma_bf16_ss(tmem + 256 + g * 128, smem_desc_sw128(pbuf + aoff, 16, 1024),
+          mma_f16kind_ss(tmem + 256 + g * 128, smem_desc_sw128(pbuf + aoff, 16, 1024),
                       smem_desc_sw128(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
                       (n > 0 || ks > 0) ? 1u : 0u);
         }
