@@ -144,18 +144,6 @@ __device__ __forceinline__ void mma_f16kind_ss(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16. A is M lanes x K 16-bit
-// elements, two consecutive K elements per 32-bit column (lower one in the
-// low half); a_tmem is the address of its first column.
-__device__ __forceinline__ void mma_f16kind_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Arrive on an mbarrier once every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
