@@ -73,6 +73,31 @@ def test_host_side_rejections_before_any_cuda_call(pkv):
                                   16, 8, 128, 256, 0.1, nul, nul, 0, nul) == -1
 
 
+@pytest.mark.parametrize("suffix", ["", "_f16"])
+def test_typed_entry_points_share_host_checks(pkv, suffix):
+    """The bf16 and fp16 entry points run the same host-side checks."""
+    lib = pkv._lib
+    nul = None
+    dec = getattr(lib, "pkv_decode" + suffix)
+    args = [nul, 2048, nul, nul, 16, nul, 16, nul, 4]
+    assert dec(*args, 16, 8, 64, 256, 4096, 0.1, nul, nul, 0, nul) == -2
+    assert dec(*args, 16, 8, 128, 256, 4096, 0.1, nul, nul, 0, nul) == -1
+    assert dec(nul, 2048, nul, nul, 16, nul, 16, nul, 0, 16, 8, 128, 256, 4096, 0.1, nul, nul, 0, nul) == 0
+    pre = getattr(lib, "pkv_prefill_varlen" + suffix)
+    assert pre(nul, 2048, 10, nul, nul, 1024, 10, nul, nul, 0, nul, nul, 10, 10, nul, 0, 1,
+               16, 8, 96, 256, 0.1, nul, nul, 0, nul) == -2
+    assert pre(nul, 2048, 10, nul, nul, 1024, 10, nul, nul, 0, nul, nul, 10, 10, nul, 0, 1,
+               16, 8, 128, 256, 0.1, nul, nul, 0, nul) == -1
+    sd = getattr(lib, "pkv_store_decode" + suffix)
+    # new-row pointers are checked before the decode arguments
+    assert sd(nul, 2048, nul, 4096, nul, 4096, nul, nul, nul, 16, nul, 16, nul, 4, 16, 8, 128, 256, 4096, 0.1,
+              nul, nul, 0, nul) == -1
+    # a new-row stride shorter than the row
+    one = ctypes.c_void_p(16)
+    assert sd(nul, 2048, one, 512, one, 4096, one, nul, nul, 16, nul, 16, nul, 4, 16, 8, 128, 256, 4096, 0.1,
+              nul, nul, 0, nul) == -3
+
+
 def test_workspace_sizes(pkv):
     assert pkv.pkv_decode_workspace_bytes(0, 4096) == 0
     a = pkv.pkv_decode_workspace_bytes(256, 4096)
