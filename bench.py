@@ -244,6 +244,8 @@ def run_ours(args, rank, world, dev):
            "roofline": roof, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
     if rank == 0 and not args.no_prefill:
         res["prefill"] = run_prefill(pkv, args, dev, bf16)
+    if rank == 0:
+        res["tiny_decode"] = run_tiny(pkv, args, dev)
     if rank == 0 and not args.no_sweep:
         res["sweep"] = run_sweep(pkv, args, dev, hbm)
         res["padded_graph"] = run_padded_graph(pkv, args, dev, hbm)
@@ -382,6 +384,60 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
                      "l2": "256 MB buffer written, then another 256 MB read, between launches"}
     assert pkv.pkv_device_error() == 0
     return res
+
+
+def run_tiny(pkv, args, dev):
+    """The 4-sequence decode step (contexts 37/256/300/511): latency in us of
+    store + decode, eager launches and one graph replay."""
+    wl = W.tiny_decode()
+    gen = W.make_generator(wl.seed, dev)
+    shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
+    kc, vc = W.normal(shape, gen, dev), W.normal(shape, gen, dev)
+    B = len(wl.seqs)
+    _, q, k, v = W.fused_qkv(B, gen, dev)
+    m = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE)
+    slot, ctx = torch.from_numpy(m["slot_mapping"]).to(dev), torch.from_numpy(m["context_lens"]).to(dev)
+    bt = torch.from_numpy(m["block_tables"]).to(dev)
+    ws = pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev)
+    out = torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        pkv.pkv_store_kvcache(k, v, kc, vc, slot)
+        pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws, out=out)
+
+    reps = max(10, min(args.steps, 200))
+    for _ in range(args.warmup):
+        step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    eager_us = a.elapsed_time(b) * 1e3 / reps
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    graph_us = a.elapsed_time(b) * 1e3 / reps
+    if pkv.pkv_device_error():
+        raise RuntimeError("device error word set by the tiny decode")
+    return {"workload": "tiny_decode_b4_ctx37/256/300/511: store 4 tokens + decode", "eager_us_per_step":
+            round(eager_us, 2), "graph_us_per_step": round(graph_us, 2), "steps": reps,
+            "note": "latency-bound (4.5 MB of K/V); back-to-back steps, CUDA events"}
 
 
 def run_padded_graph(pkv, args, dev, hbm_peak):
@@ -596,6 +652,24 @@ def ncu_case(kind):
             pkv.pkv_prefill_varlen(q, d(m["cu_seqlens_q"]), d(m["cu_seqlens_k"]), m["max_seqlen_q"],
                                    m["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc, block_tables=d(m["block_tables"]))
         units = _prefill_flops(seqs)
+    elif kind == "sweep":
+        # the 28-layer sweep, one eager pass (store + decode per layer): 56 launches
+        # on a 54 GB cache, for a one-metric launch list only
+        wl = W.sweep_decode()
+        L, B = wl.num_layers, len(wl.seqs)
+        gen = W.make_generator(wl.seed, dev)
+        kv = W.normal_bf16((2, L, wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM), gen, dev)
+        m = pkv.metadata.prepare_decode(wl.seqs, W.BLOCK_SIZE, table_width=W.MAX_MODEL_LEN // W.BLOCK_SIZE)
+        d = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
+        slot, ctx, bt = d(m["slot_mapping"]), d(m["context_lens"]), d(m["block_tables"])
+        ws = pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev)
+        qkv = [W.fused_qkv(B, gen, dev) for _ in range(L)]
+        torch.cuda.synchronize()
+        for l in range(L):
+            _, q, k, v = qkv[l]
+            pkv.pkv_store_kvcache(k, v, kv[0, l], kv[1, l], slot)
+            pkv.pkv_decode(q, kv[0, l], kv[1, l], bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
+        units = L * int(m["context_lens"].astype(np.int64).sum()) * W.HKV * W.HEAD_DIM * 4
     elif kind == "store":
         gen = W.make_generator(3, dev)
         N = 16384
@@ -696,7 +770,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-f16", action="store_true", help="skip the fp16 entry points' timings")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "store"])
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "store", "sweep"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.ncu_case:
