@@ -6,20 +6,22 @@
 // last position), query head h on kv head h/2.
 //
 // GB300 design (HBM-bound: 4 KB of K+V per token for 8 kv heads x 128 dims):
-//  * One CTA per (logical block c, sequence b): the block's tokens are one
-//    contiguous 512 KB K region and one 512 KB V region of the cache, so the
-//    producer warp streams them with plain bulk copies (cp.async.bulk, 1-D
-//    TMA), kT tokens x 2 KB per stage, through a kStages-deep shared-memory
-//    ring guarded by mbarriers.
+//  * One CTA per (chunk c, sequence b), a chunk being `chunk` consecutive
+//    tokens inside one 256-token block (chunk = 256, 128, 64 or 32, chosen on
+//    the host so that small batches still give the GPU enough CTAs). A
+//    chunk's tokens are one contiguous K region and one V region of the
+//    cache, so the producer warp streams them with plain bulk copies
+//    (cp.async.bulk, 1-D TMA), kT tokens x 2 KB per stage, through a
+//    kStages-deep shared-memory ring guarded by mbarriers.
 //  * Consumer warp w owns kv head w and both query heads 2w, 2w+1 that read
 //    it, so each K/V byte is loaded once for the whole GQA group. Lane l holds
 //    dims 4l..4l+3. Per stage every lane forms 2*kT partial dot products and a
 //    transposed butterfly (2*kT-1 shuffles for 2*kT results) leaves lane l
 //    with one complete logit; softmax statistics are half-warp reductions.
 //  * Split-KV merge without a second launch: each CTA writes (m, l, o) for its
-//    block to the workspace, and the CTA that finishes last for a sequence
+//    chunk to the workspace, and the CTA that finishes last for a sequence
 //    (atomic ticket, no waiting) merges them and resets the ticket to zero.
-//    Sequences with a single block write the output directly.
+//    Sequences with a single chunk write the output directly.
 //  * Logits are kept in the log2 domain (q is pre-scaled by scale*log2(e))
 //    and exponentials use ex2.approx.
 //  * The element type (bf16 or fp16) is a template parameter: it only changes
@@ -64,6 +66,7 @@ struct DecodeParams {
   const int32_t* context_lens;
   int32_t max_ctx;
   int32_t nsplit;
+  int32_t chunk;      // tokens per CTA: 256, 128, 64 or 32 (divides the block size)
   float scale_log2;
   uint16_t* out;
   int32_t* tickets;   // [num_seqs]
@@ -144,10 +147,11 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
     }
     return;
   }
-  const int nchunks = (ctx + kBlockSize - 1) / kBlockSize;
+  const int nchunks = (ctx + p.chunk - 1) / p.chunk;
   if (c >= nchunks) return;
-  const int ntok = min(kBlockSize, ctx - c * kBlockSize);
-  const int pb = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + c];
+  const int tok0 = c * p.chunk;  // first position of this chunk; the chunk lies inside one block
+  const int ntok = min(p.chunk, ctx - tok0);
+  const int pb = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + tok0 / kBlockSize];
   const bool bad_block = pb < 0 || pb >= p.num_blocks;
   const int niter = bad_block ? 0 : (ntok + kT - 1) / kT;
 
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
   if (warp == kConsumerWarps) {
     // ---------------- producer: one elected lane streams the block ----------------
     if (lane == 0 && niter > 0) {
-      const int64_t base = static_cast<int64_t>(pb) * kBlockSize * kRowBytes;
+      const int64_t base = (static_cast<int64_t>(pb) * kBlockSize + tok0 % kBlockSize) * kRowBytes;
       const uint8_t* ksrc = p.k_cache + base;
       const uint8_t* vsrc = p.v_cache + base;
       int issued = 0;
@@ -395,11 +399,25 @@ cudaError_t launch_typed(const DecodeParams& p, int32_t num_seqs, cudaStream_t s
 
 }  // namespace
 
-int decode_num_splits(int32_t max_context_len) { return (max_context_len + kBlockSize - 1) / kBlockSize; }
+// Tokens per CTA for these sizes: the largest of 256, 128, 64, 32 that still
+// gives at least kMinCtas CTAs (two resident per SM, about two waves on a
+// 152-SM GB300), else 32. A function of the call's sizes only, so the
+// workspace query and the launch always agree.
+constexpr int kMinCtas = 608;
+int decode_chunk(int32_t num_seqs, int32_t max_context_len) {
+  int chunk = kBlockSize;
+  while (chunk > 32 && static_cast<int64_t>(num_seqs) * ((max_context_len + chunk - 1) / chunk) < kMinCtas) chunk >>= 1;
+  return chunk;
+}
+
+int decode_num_splits(int32_t num_seqs, int32_t max_context_len) {
+  const int chunk = decode_chunk(num_seqs, max_context_len);
+  return (max_context_len + chunk - 1) / chunk;
+}
 
 size_t decode_workspace_bytes(int32_t num_seqs, int32_t max_context_len) {
   const size_t ns = static_cast<size_t>(num_seqs);
-  const size_t nsplit = static_cast<size_t>(decode_num_splits(max_context_len));
+  const size_t nsplit = static_cast<size_t>(decode_num_splits(num_seqs, max_context_len));
   return align_up(ns * sizeof(int32_t), 256) + align_up(ns * nsplit * kHq * sizeof(float2), 256) +
          ns * nsplit * kHq * kHeadDim * sizeof(float);
 }
@@ -427,7 +445,8 @@ cudaError_t launch_decode(const void* q, int64_t q_row_stride, const void* k_cac
   p.bt_stride = bt_stride;
   p.context_lens = context_lens;
   p.max_ctx = max_context_len;
-  p.nsplit = decode_num_splits(max_context_len);
+  p.chunk = decode_chunk(num_seqs, max_context_len);
+  p.nsplit = decode_num_splits(num_seqs, max_context_len);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.out = static_cast<uint16_t*>(out);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

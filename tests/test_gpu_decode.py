@@ -90,6 +90,20 @@ def test_ragged_contexts(pkv, ctxs):
     _decode_step(pkv, wl, "cuda", poison=True, fused=False)
 
 
+@pytest.mark.parametrize("num_seqs", [1, 5, 20, 40])
+def test_split_sizes_for_small_batches(pkv, num_seqs):
+    """Small batches split each 256-token block over several CTAs (32, 64,
+    128 or 256 tokens each, picked from num_seqs and max_context_len); every
+    split size gives the oracle's result, including a 4096-token context
+    merged from 128 partials."""
+    rng = np.random.default_rng(100 + num_seqs)
+    ctxs = [4096] + [int(x) for x in rng.integers(1, 4097, size=num_seqs - 1)]
+    nb = sum(W.blocks_for(c) for c in ctxs) + 3
+    wl = W.Workload(f"split_{num_seqs}", 200 + num_seqs, W._decode_seqs(ctxs, nb, rng), nb, "decode")
+    sample = list(range(min(num_seqs, 6)))
+    _decode_step(pkv, wl, "cuda", sample=sample, poison=True)
+
+
 def test_batched_decode_full_size(pkv):
     """256 sequences, context 512..4096, 8192-block pool: sampled sequences
     (shortest, longest and a random spread) against the oracle."""
