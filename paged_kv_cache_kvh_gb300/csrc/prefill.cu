@@ -28,6 +28,7 @@
 // grows by more than 8 (2^8 headroom in fp32/bf16), so O is rescaled rarely.
 // The last V tile's rows beyond the sequence are zeroed in shared memory
 // before use, so stale or NaN cache contents never reach the product.
+// The producer also warms L2 with the Q tiles of the CTA one wave ahead.
 // The element type (bf16 or fp16) is a template parameter: it sets the
 // tensor-core operand format, the tensor maps' element type and how P and
 // the output are rounded; P <= 2^8 fits either type.
@@ -80,6 +81,7 @@ struct PrefillParams {
   int32_t total_k;  // rows of contiguous k/v (ignored when paged)
   int32_t paged;
   float scale_log2;
+  int32_t ahead;  // block index distance to the CTA likely to run next on this SM (the SM count)
   uint16_t* out;  // 16-bit elements of the call's type
   unsigned int* err;
 };
@@ -198,6 +200,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(dst, tm, 0, hk, row, bar(kBarKvFull + slot));
         tma_load_3d(dst + kHalfBytes, tm, 64, hk, row, bar(kBarKvFull + slot));
         ++issued;
+      }
+    }
+    if (lane == 0) {
+      // Warm L2 with the Q tiles of the CTA launched a wave after this one:
+      // Q is read once, so its first load would otherwise come from HBM (its
+      // K/V tiles are shared with the sequence's other query tiles and are
+      // usually in L2 already).
+      const int nb = static_cast<int>(blockIdx.x) + p.ahead;
+      if (nb < static_cast<int>(gridDim.x)) {
+        const int qt2 = p.max_q_tiles - 1 - nb / per_tile;
+        const int b2 = (nb % per_tile) / kHkv, hk2 = (nb % per_tile) % kHkv;
+        const int q0 = p.cu_q[b2], q1 = p.cu_q[b2 + 1];
+        if (qt2 * kBM < q1 - q0) {
+          for (int g = 0; g < kGroup; ++g) {
+            tma_prefetch_l2_3d(&tm_q, 0, kGroup * hk2 + g, q0 + qt2 * kBM);
+            tma_prefetch_l2_3d(&tm_q, 64, kGroup * hk2 + g, q0 + qt2 * kBM);
+          }
+        }
       }
     }
     issued = __shfl_sync(0xffffffffu, issued, 0);
@@ -535,6 +555,12 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
   p.total_k = paged ? 0 : total_k;
   p.paged = paged ? 1 : 0;
   p.scale_log2 = scale * 1.4426950408889634f;
+  {
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
+    p.ahead = sms;
+  }
   p.out = static_cast<uint16_t*>(out);
   p.err = err;
   const int64_t nblocks = static_cast<int64_t>(p.max_q_tiles) * num_seqs * kHkv;
