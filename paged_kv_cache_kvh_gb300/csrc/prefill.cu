@@ -63,7 +63,8 @@ constexpr int kBarPReady = kBarSFull + 2;         // +g
 constexpr int kBarOFinal = kBarPReady + 2;
 constexpr int kBarVTail = kBarOFinal + 1;
 constexpr int kBarDrain = kBarVTail + 1;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarStaged = kBarDrain + 1;          // the 8 softmax warps have staged their O rows
+constexpr int kNumBars = kBarStaged + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
 constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 
@@ -152,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool v_tail = tail_keys < kBN;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), (i == kBarPReady || i == kBarPReady + 1) ? 4 : 1);
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(bar(i), (i == kBarPReady || i == kBarPReady + 1) ? 4 : (i == kBarStaged ? 8 : 1));
     *s_abort = 0;
     mbar_fence_init();
   }
@@ -432,28 +434,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(kBarPReady + g));
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(kBarOFinal), 0, s_abort, p.err));
+    // Epilogue. Every product is complete, so the two P buffers (64 KB) are
+    // free: each thread stages its normalised O row there (the two query heads
+    // of a row side by side, 512 B, 16-byte chunks rotated by the row to spread
+    // the banks), then each warp stores whole rows: the two heads of a query
+    // row are adjacent in out, so one warp instruction writes 512 contiguous
+    // bytes instead of touching 32 rows.
+    const uint32_t stage = sbase + kOffP;
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool row_ok = row < rows_valid;
-      uint16_t* orow = p.out + (static_cast<int64_t>(cq0 + r0 + row) * kHq + (kGroup * hk + g)) * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         tmem_ld32(tO + c * 32, r);
         tmem_wait_ld();
         tmem_reg_fence(r);
-        if (row_ok) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 w;
-            w.x = Ops::pack(__uint_as_float(r[j + 0]) * inv, __uint_as_float(r[j + 1]) * inv);
-            w.y = Ops::pack(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv);
-            w.z = Ops::pack(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv);
-            w.w = Ops::pack(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + j) = w;
-          }
+        for (int j = 0; j < 32; j += 8) {
+          const int q = g * 16 + c * 4 + j / 8;  // 16-byte chunk of the 512-byte row
+          sts128(stage + row * 512 + ((q ^ (row & 31)) << 4),
+                 Ops::pack(__uint_as_float(r[j + 0]) * inv, __uint_as_float(r[j + 1]) * inv),
+                 Ops::pack(__uint_as_float(r[j + 2]) * inv, __uint_as_float(r[j + 3]) * inv),
+                 Ops::pack(__uint_as_float(r[j + 4]) * inv, __uint_as_float(r[j + 5]) * inv),
+                 Ops::pack(__uint_as_float(r[j + 6]) * inv, __uint_as_float(r[j + 7]) * inv));
         }
+      }
+    }
+    // all 8 softmax warps arrive, whatever happened, so the wait below always ends
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarStaged));
+    const bool staged = __all_sync(0xffffffffu, wait_or_abort(bar(kBarStaged), 0, s_abort, p.err));
+    if (ok && staged) {
+      uint16_t* obase = p.out + (static_cast<int64_t>(cq0 + r0) * kHq + kGroup * hk) * kHeadDim + lane * 8;
+      for (int rr = warp - 2; rr < rows_valid; rr += 8) {
+        uint32_t a, b2, c2, d;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(a), "=r"(b2), "=r"(c2), "=r"(d)
+                     : "r"(stage + rr * 512 + ((lane ^ (rr & 31)) << 4)));
+        *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(rr) * kHq * kHeadDim) = make_uint4(a, b2, c2, d);
       }
     }
   }
