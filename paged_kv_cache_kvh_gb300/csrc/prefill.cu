@@ -152,11 +152,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tail_keys = Lk - (n_tiles - 1) * kBN;  // valid keys in the last tile (1..128)
   const bool v_tail = tail_keys < kBN;
 
+  auto k_row = [&](int n) -> int {
+    if (!p.paged) return ck0 + n * kBN;
+    int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (n * kBN) / kBlockSize];
+    if (blk < 0 || blk >= p.num_blocks) {
+      flag_error(p.err, PKV_DEVERR_BAD_BLOCK);
+      blk = 0;
+    }
+    return blk * kBlockSize + (n * kBN) % kBlockSize;
+  };
+  // ring item i: K_{i/2} (even i) or V_{i/2} (odd i), into slot i % kKvSlots
+  auto load_kv = [&](int i) {
+    const int slot = i % kKvSlots;
+    const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
+    const int row = k_row(i >> 1);
+    const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
+    mbar_arrive_expect_tx(bar(kBarKvFull + slot), kTileBytes);
+    tma_load_3d(dst, tm, 0, hk, row, bar(kBarKvFull + slot));
+    tma_load_3d(dst + kHalfBytes, tm, 64, hk, row, bar(kBarKvFull + slot));
+  };
+
+  // Thread 0 is the producer's issuing lane: right after initialising the
+  // barriers it starts the Q loads and fills the K/V ring, before the TMEM
+  // allocation and the CTA barrier, so the copies are in flight sooner.
+  int early = 0;  // ring items issued here (thread 0 only)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
       mbar_init(bar(i), (i == kBarPReady || i == kBarPReady + 1) ? 4 : (i == kBarStaged ? 8 : 1));
     *s_abort = 0;
     mbar_fence_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    mbar_arrive_expect_tx(bar(kBarQ), 2 * kTileBytes);
+    for (int g = 0; g < kGroup; ++g) {
+      const uint32_t dst = sbase + kOffQ + g * kTileBytes;
+      tma_load_3d(dst, &tm_q, 0, kGroup * hk + g, cq0 + r0, bar(kBarQ));
+      tma_load_3d(dst + kHalfBytes, &tm_q, 64, kGroup * hk + g, cq0 + r0, bar(kBarQ));
+    }
+    for (; early < kKvSlots && early < 2 * n_tiles; ++early) load_kv(early);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(s_tmem), 512);
@@ -167,40 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  auto k_row = [&](int n) -> int {
-    if (!p.paged) return ck0 + n * kBN;
-    int blk = p.block_tables[static_cast<int64_t>(b) * p.bt_stride + (n * kBN) / kBlockSize];
-    if (blk < 0 || blk >= p.num_blocks) {
-      flag_error(p.err, PKV_DEVERR_BAD_BLOCK);
-      blk = 0;
-    }
-    return blk * kBlockSize + (n * kBN) % kBlockSize;
-  };
-
   if (warp == 0) {
     // =========================== TMA producer ===========================
-    int issued = 0;
+    int issued = early;
     if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(bar(kBarQ), 2 * kTileBytes);
-      for (int g = 0; g < kGroup; ++g) {
-        const uint32_t dst = sbase + kOffQ + g * kTileBytes;
-        tma_load_3d(dst, &tm_q, 0, kGroup * hk + g, cq0 + r0, bar(kBarQ));
-        tma_load_3d(dst + kHalfBytes, &tm_q, 64, kGroup * hk + g, cq0 + r0, bar(kBarQ));
-      }
-      for (int i = 0; i < 2 * n_tiles; ++i) {
+      for (int i = early; i < 2 * n_tiles; ++i) {
         const int slot = i % kKvSlots;
         if (i >= kKvSlots && !wait_or_abort(bar(kBarKvFree + slot), ((i / kKvSlots) - 1) & 1, s_abort, p.err))
           break;
-        const int n = i >> 1;
-        const CUtensorMap* tm = (i & 1) ? &tm_v : &tm_k;
-        const int row = k_row(n);
-        const uint32_t dst = sbase + kOffKV + slot * kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarKvFull + slot), kTileBytes);
-        tma_load_3d(dst, tm, 0, hk, row, bar(kBarKvFull + slot));
-        tma_load_3d(dst + kHalfBytes, tm, 64, hk, row, bar(kBarKvFull + slot));
+        load_kv(i);
         ++issued;
       }
     }
