@@ -105,6 +105,25 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   }
 }
 
+// 8-column TMEM load / store (32 lanes x 8 x 32 bit), for the rare O rescale
+// while the tile's 128 probabilities are still held in registers.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+// keeps uses of a tmem_ld8 result after the tcgen05.wait::ld that completes it
+__device__ __forceinline__ void tmem_reg_fence8(uint32_t (&r)[8]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -401,39 +420,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // P = 2^(s*sl2 - m_use), rounded to the element type, into the swizzled K-major A tile
       const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
       const uint64_t negm2 = f32x2_pack(-m_use, -m_use);
-      uint64_t lsum2 = f32x2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        float e[8];
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
+        for (int j = c * 8; j < c * 8 + 8; j += 2) {
           float a0, a1;
-          f32x2_unpack(f32x2_fma(f32x2_pack(s[c * 8 + j], s[c * 8 + j + 1]), sl2x2, negm2), a0, a1);
-          e[j] = ex2_approx(a0);
-          e[j + 1] = ex2_approx(a1);
-          lsum2 = f32x2_add(lsum2, f32x2_pack(e[j], e[j + 1]));
+          f32x2_unpack(f32x2_fma(f32x2_pack(s[j], s[j + 1]), sl2x2, negm2), a0, a1);
+          s[j] = ex2_approx(a0);
+          s[j + 1] = ex2_approx(a1);
         }
         const int half = c >> 3;
         const uint32_t addr = prow + half * kHalfBytes + (((c & 7) ^ swz) << 4);
+        const float* e = s + c * 8;
         sts128(addr, Ops::pack(e[0], e[1]), Ops::pack(e[2], e[3]), Ops::pack(e[4], e[5]), Ops::pack(e[6], e[7]));
-      }
-      {
-        float l0, l1;
-        f32x2_unpack(lsum2, l0, l1);
-        l += l0 + l1;
       }
       m = m_use;
       // rescale the running output (PV_g(n-1) is complete: S_g(n) was issued after it)
       if (n > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tO + c * 32, r);
+#pragma unroll 1
+        for (int c = 0; c < 16; ++c) {
+          uint32_t r[8];
+          tmem_ld8(tO + c * 8, r);
           tmem_wait_ld();
-          tmem_reg_fence(r);
+          tmem_reg_fence8(r);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-          tmem_st32(tO + c * 32, r);
+          for (int j = 0; j < 8; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+          tmem_st8(tO + c * 8, r);
         }
         tmem_wait_st();
       }
@@ -441,6 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarPReady + g));
+      // The row sum is not needed for P: add it up after P is handed over.
+      {
+        uint64_t acc[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = f32x2_pack(s[2 * a], s[2 * a + 1]);
+#pragma unroll
+        for (int j = 8; j < 128; j += 8)
+#pragma unroll
+          for (int a = 0; a < 4; ++a) acc[a] = f32x2_add(acc[a], f32x2_pack(s[j + 2 * a], s[j + 2 * a + 1]));
+        float t0, t1, t2, t3, t4, t5, t6, t7;
+        f32x2_unpack(acc[0], t0, t1);
+        f32x2_unpack(acc[1], t2, t3);
+        f32x2_unpack(acc[2], t4, t5);
+        f32x2_unpack(acc[3], t6, t7);
+        l += ((t0 + t1) + (t2 + t3)) + ((t4 + t5) + (t6 + t7));
+      }
     }
     if (ok) ok = __all_sync(0xffffffffu, wait_or_abort(bar(kBarOFinal), 0, s_abort, p.err));
     // Epilogue. Every product is complete, so the two P buffers (64 KB) are
