@@ -83,6 +83,16 @@ def _traffic(kernel_file, units_now, case=None):
     return e["dram_bytes_per_launch"] * (units_now / e["units"]) if e.get("units") else e["dram_bytes_per_launch"]
 
 
+def _traffic_launch(kernel_file, case):
+    """Which launch of a workload a per-workload capture measured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        c = json.load(f).get(kernel_file, {}).get("cases", {}).get(case)
+    return None if c is None else c.get("launch")
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -379,7 +389,8 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
                                   "peak_source": ("measured bf16 dense (cuBLAS burst) x nominal fp16/bf16 ratio 1"
                                                   if f16 else "measured bf16 dense (cuBLAS burst)"),
                                   "traffic": None if f16 else _traffic("prefill.cu", flops, case=name),
-                                  "traffic_note": "ncu DRAM bytes of one launch (the workload's first call)"},
+                                  "traffic_note": "ncu DRAM bytes of one launch: "
+                                                  + str(_traffic_launch("prefill.cu", name))},
                      "store_ms": round(t_st, 4), "store_gbs": round(store_bytes / (t_st * 1e-3) / 1e9, 1),
                      "l2": "256 MB buffer written, then another 256 MB read, between launches"}
     assert pkv.pkv_device_error() == 0
@@ -637,9 +648,13 @@ def ncu_case(kind):
         for _ in range(3):
             pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
         units = int(m["context_lens"].astype(np.int64).sum()) * W.HKV * W.HEAD_DIM * 4
-    elif kind in ("prefill", "prefill_prefix"):
-        wl = W.varlen_prefill() if kind == "prefill" else W.prefix_prefill()
-        seqs = wl.seqs[0]
+    elif kind in ("prefill", "prefill_prefix", "prefill_chunked"):
+        # the workload's first call; for the chunked workload call 9, a full
+        # 5000-token chunk continuing 5000 cached tokens (whatever values the
+        # seeded pool holds stand in for the keys the earlier call stored)
+        wl = {"prefill": W.varlen_prefill, "prefill_prefix": W.prefix_prefill,
+              "prefill_chunked": W.chunked_prefill}[kind]()
+        seqs = wl.seqs[9 if kind == "prefill_chunked" else 0]
         gen = W.make_generator(wl.seed, dev)
         shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
         kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
@@ -770,7 +785,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-f16", action="store_true", help="skip the fp16 entry points' timings")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "store", "sweep"])
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "prefill_chunked", "store", "sweep"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.ncu_case:

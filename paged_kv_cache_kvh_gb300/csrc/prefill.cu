@@ -67,6 +67,7 @@ constexpr int kBarStaged = kBarDrain + 1;          // the 8 softmax warps have s
 constexpr int kNumBars = kBarStaged + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
 constexpr size_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory above the 227 KB a CTA can opt into");
 
 struct PrefillParams {
   const int32_t* cu_q;
