@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
+  __syncwarp();  // warp 0 arrives converged, after thread 0 has initialised the barriers
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
@@ -499,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // all 8 softmax warps arrive, whatever happened, so the wait below always ends
+    // all 8 softmax warps arrive, whatever happened, so the wait below (and
+    // warp 1's before releasing TMEM) always ends; every tensor-memory read of
+    // this warp is complete here
+    tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kBarStaged));
     const bool staged = __all_sync(0xffffffffu, wait_or_abort(bar(kBarStaged), 0, s_abort, p.err));
@@ -515,9 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  tc_fence_before();
-  __syncthreads();
   if (warp == 1) {
+    // TMEM is released after every softmax warp's last tensor-memory read
+    // (they all arrive on kBarStaged once O is staged); no CTA-wide barrier,
+    // so no role waits at one with some of its lanes still busy. The wait is
+    // time-bounded but ignores the abort flag: the softmax warps always arrive.
+    __syncwarp();
+    mbar_wait(bar(kBarStaged), 0, p.err);
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
