@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
     }
     mbar_fence_init();
   }
+  __syncwarp();  // every warp reaches each CTA barrier converged
   __syncthreads();
 
   float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -325,12 +326,14 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
 
   if (nchunks == 1) return;
   // ---------------- split-KV merge by the last CTA of this sequence ----------------
+  __syncwarp();  // the producer warp's lane 0 streamed alone: reconverge first
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     const int prev = atomicAdd(p.tickets + b, 1);
     *s_last = (prev == nchunks - 1) ? 1 : 0;
   }
+  __syncwarp();
   __syncthreads();
   if (*s_last == 0) return;
   __threadfence();
