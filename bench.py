@@ -733,6 +733,26 @@ def _oracle_step(orc, s):
                num_kv_heads=W.HKV)
 
 
+def _cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(c=None, budget_s=10.0, num_sample=16):
     import oracle
     orc = oracle.default()
@@ -746,7 +766,7 @@ def cpu_baseline(c=None, budget_s=10.0, num_sample=16):
         if el >= budget_s or reps >= 1000:
             break
     return {"value": round(s["kv_bytes"] * reps / el / 1e9, 4), "unit": UNIT, "cores": orc.num_threads(),
-            "kind": "oracle", "sample": f"store + decode of the first {num_sample} of the 256 sequences "
+            "cpu_model": _cpu_model(), "kind": "oracle", "sample": f"store + decode of the first {num_sample} of the 256 sequences "
                                        f"(fp64 C oracle), repeated {reps}x over {el:.1f} s"}
 
 
@@ -768,6 +788,7 @@ def run_reference(args):
             "config": {"workload": "batched_decode_b256_ctx512-4096: store_kvcache(256 tokens) + GQA decode",
                        "sample_seqs": args.ref_sample},
             "cpu_baseline": {"value": val, "unit": UNIT, "kind": "oracle", "cores": orc.num_threads(),
+                             "cpu_model": _cpu_model(),
                              "sample": f"each step: store + decode of the first {args.ref_sample} of the 256 "
                                        f"sequences with the fp64 C oracle"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
