@@ -29,6 +29,10 @@
 // The last V tile's rows beyond the sequence are zeroed in shared memory
 // before use, so stale or NaN cache contents never reach the product.
 // The producer also warms L2 with the Q tiles of the CTA one wave ahead.
+// Epilogue: O is staged in the (then free) P buffers and leaves as whole
+// 512-byte rows (both heads of a query row); warp 1 releases TMEM once every
+// softmax warp has staged its rows. There is no CTA-wide barrier at the end,
+// so no role ever waits at one with lanes still busy in their role.
 // The element type (bf16 or fp16) is a template parameter: it sets the
 // tensor-core operand format, the tensor maps' element type and how P and
 // the output are rounded; P <= 2^8 fits either type.
