@@ -399,7 +399,8 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
 
 def run_tiny(pkv, args, dev):
     """The 4-sequence decode step (contexts 37/256/300/511): latency in us of
-    store + decode, eager launches and one graph replay."""
+    store + decode, eager launches and one graph replay; also the fused
+    store + decode launch (pkv_store_decode) replayed in a graph."""
     wl = W.tiny_decode()
     gen = W.make_generator(wl.seed, dev)
     shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
@@ -411,44 +412,54 @@ def run_tiny(pkv, args, dev):
     bt = torch.from_numpy(m["block_tables"]).to(dev)
     ws = pkv.decode_workspace(B, W.MAX_MODEL_LEN, dev)
     out = torch.empty(B, W.HQ, W.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+    reps = max(10, min(args.steps, 200))
+
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / n
+
+    def graph_of(fn):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
 
     def step():
         pkv.pkv_store_kvcache(k, v, kc, vc, slot)
         pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws, out=out)
 
-    reps = max(10, min(args.steps, 200))
+    def fused_step():
+        pkv.pkv_store_decode(q, k, v, slot, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws, out=out)
+
     for _ in range(args.warmup):
         step()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    a.record()
-    for _ in range(reps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    eager_us = a.elapsed_time(b) * 1e3 / reps
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        step()
-    torch.cuda.current_stream().wait_stream(s)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        step()
+    eager_us = timed(step, reps)
+    g = graph_of(step)
     for _ in range(args.warmup):
         g.replay()
-    torch.cuda.synchronize()
-    a.record()
-    for _ in range(reps):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    graph_us = a.elapsed_time(b) * 1e3 / reps
+    graph_us = timed(g.replay, reps)
+    gf = graph_of(fused_step)
+    for _ in range(args.warmup):
+        gf.replay()
+    fused_us = timed(gf.replay, reps)
     if pkv.pkv_device_error():
         raise RuntimeError("device error word set by the tiny decode")
     return {"workload": "tiny_decode_b4_ctx37/256/300/511: store 4 tokens + decode", "eager_us_per_step":
-            round(eager_us, 2), "graph_us_per_step": round(graph_us, 2), "steps": reps,
-            "note": "latency-bound (4.5 MB of K/V); back-to-back steps, CUDA events"}
+            round(eager_us, 2), "graph_us_per_step": round(graph_us, 2),
+            "fused_graph_us_per_step": round(fused_us, 2), "steps": reps,
+            "note": "latency-bound (4.5 MB of K/V); back-to-back steps, CUDA events; fused = pkv_store_decode, "
+                    "one launch"}
 
 
 def run_padded_graph(pkv, args, dev, hbm_peak):
