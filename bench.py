@@ -362,34 +362,44 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
                               slot=torch.from_numpy(m["slot_mapping"]).to(dev),
                               cq=torch.from_numpy(m["cu_seqlens_q"]).to(dev),
                               ck=torch.from_numpy(m["cu_seqlens_k"]).to(dev),
-                              bt=torch.from_numpy(m["block_tables"]).to(dev)))
-        pre_ms, st_ms = [], []
+                              bt=torch.from_numpy(m["block_tables"]).to(dev),
+                              # the step's tile plan, built on the host with its metadata (untimed)
+                              plan=pkv.pkv_prefill_plan(m["cu_seqlens_q"], m["cu_seqlens_k"], dev)))
         for it in range(iters + 3):
             for cl in calls:
                 _flush_l2(flush)
-                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0, e1, e2, e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(5))
                 e0.record()
                 pkv.pkv_store_kvcache(cl["k"], cl["v"], kc, vc, cl["slot"])
                 e1.record()
                 prefill(cl["q"], cl["cq"], cl["ck"], cl["m"]["max_seqlen_q"], cl["m"]["max_seqlen_k"],
-                        W.SCALE, k_cache=kc, v_cache=vc, block_tables=cl["bt"])
+                        W.SCALE, k_cache=kc, v_cache=vc, block_tables=cl["bt"], plan=cl["plan"])
                 e2.record()
+                _flush_l2(flush)
+                e3.record()
+                prefill(cl["q"], cl["cq"], cl["ck"], cl["m"]["max_seqlen_q"], cl["m"]["max_seqlen_k"],
+                        W.SCALE, k_cache=kc, v_cache=vc, block_tables=cl["bt"])
+                e4.record()
                 if it >= 3:
-                    cl.setdefault("ev", []).append((e0, e1, e2))
+                    cl.setdefault("ev", []).append((e0, e1, e2, e3, e4))
         torch.cuda.synchronize()
         flops = sum(cl["flops"] for cl in calls)
-        t_pre = sum(e1.elapsed_time(e2) for cl in calls for (_, e1, e2) in cl["ev"]) / iters
-        t_st = sum(e0.elapsed_time(e1) for cl in calls for (e0, e1, _) in cl["ev"]) / iters
+        t_pre = sum(ev[1].elapsed_time(ev[2]) for cl in calls for ev in cl["ev"]) / iters
+        t_noplan = sum(ev[3].elapsed_time(ev[4]) for cl in calls for ev in cl["ev"]) / iters
+        t_st = sum(ev[0].elapsed_time(ev[1]) for cl in calls for ev in cl["ev"]) / iters
         store_bytes = sum(4 * int((cl["m"]["slot_mapping"] >= 0).sum()) * W.HKV * W.HEAD_DIM * 2 for cl in calls)
         tf = flops / (t_pre * 1e-3) / 1e12
         res[name] = {"calls": len(calls), "tokens": sum(cl["T"] for cl in calls), "gflop": round(flops / 1e9, 2),
                      "prefill_ms": round(t_pre, 4), "tflops": round(tf, 1),
+                     "plan": "host tile plan per call (pkv_prefill_plan), built with the metadata, untimed",
+                     "no_plan": {"prefill_ms": round(t_noplan, 4),
+                                 "tflops": round(flops / (t_noplan * 1e-3) / 1e12, 1)},
                      "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(tf, 1),
                                   "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
                                   "peak_source": ("measured bf16 dense (cuBLAS burst) x nominal fp16/bf16 ratio 1"
                                                   if f16 else "measured bf16 dense (cuBLAS burst)"),
                                   "traffic": None if f16 else _traffic("prefill.cu", flops, case=name),
-                                  "traffic_note": "ncu DRAM bytes of one launch: "
+                                  "traffic_note": "ncu DRAM bytes of one planned launch: "
                                                   + str(_traffic_launch("prefill.cu", name))},
                      "store_ms": round(t_st, 4), "store_gbs": round(store_bytes / (t_st * 1e-3) / 1e9, 1),
                      "l2": "256 MB buffer written, then another 256 MB read, between launches"}
@@ -674,9 +684,11 @@ def ncu_case(kind):
         m = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
         d = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
         pkv.pkv_store_kvcache(k, v, kc, vc, d(m["slot_mapping"]))
+        plan = pkv.pkv_prefill_plan(m["cu_seqlens_q"], m["cu_seqlens_k"], dev)
         for _ in range(3):
             pkv.pkv_prefill_varlen(q, d(m["cu_seqlens_q"]), d(m["cu_seqlens_k"]), m["max_seqlen_q"],
-                                   m["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc, block_tables=d(m["block_tables"]))
+                                   m["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc, block_tables=d(m["block_tables"]),
+                                   plan=plan)
         units = _prefill_flops(seqs)
     elif kind == "sweep":
         # the 28-layer sweep, one eager pass (store + decode per layer): 56 launches

@@ -132,8 +132,18 @@ int pkv_store_kvcache(const void* k, int64_t k_row_stride, const void* v, int64_
  *        cu_seqlens_q[num_seqs] <= total_q and, in contiguous mode,
  *        cu_seqlens_k[num_seqs] <= total_k.
  * q, k, v, k_cache, v_cache must be 16-byte aligned and their row strides
- * multiples of 8 elements (tensor-memory-access rules). workspace may be
- * NULL when pkv_prefill_workspace_bytes() is 0.
+ * multiples of 8 elements (tensor-memory-access rules).
+ *
+ * workspace: NULL, or a tile plan -- workspace_bytes/4 int32 items written by
+ *   pkv_prefill_plan for these cu_seqlens and copied to device memory (4-byte
+ *   aligned, workspace_bytes a multiple of 4, at most 2^28 items). Without a
+ *   plan every (128-row query tile, sequence) pair up to max_seqlen_q is
+ *   launched, longest key ranges first, and the tiles past a sequence's end
+ *   exit at once; with a plan exactly the plan's items are launched, in its
+ *   order. Items past a sequence's end are skipped, items naming a sequence
+ *   >= num_seqs are skipped and set PKV_DEVERR_BAD_SEQLEN (a stale plan gives
+ *   missing rows, never an out-of-bounds access); results are identical with
+ *   and without a plan.
  */
 int pkv_prefill_varlen(const void* q, int64_t q_row_stride, int32_t total_q, const void* k, const void* v,
                        int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
@@ -158,8 +168,27 @@ int pkv_prefill_varlen_f16(const void* q, int64_t q_row_stride, int32_t total_q,
                            int32_t head_dim, int32_t block_size, float softmax_scale, void* out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes pkv_prefill_varlen(_f16) needs for these sizes (may be 0). */
+/* Workspace bytes pkv_prefill_varlen(_f16) needs for these sizes (0: none;
+ * an optional tile plan may be passed in its place). */
 size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
+
+/*
+ * pkv_prefill_plan -- host-side tile plan for pkv_prefill_varlen(_f16), built
+ * once per engine step from the host copies of the step's cu_seqlens (the
+ * pages' prepare_prefill builds them on the host) and reused by every layer.
+ *
+ * Writes one int32 per (128-row query tile qt, sequence b) pair that holds
+ * query rows, encoded (qt << 16) | b, ordered by the number of 128-key tiles
+ * the query tile attends to, most first (ties: lower b, then higher qt), so the
+ * longest tiles start first. h_cu_seqlens_q / h_cu_seqlens_k: [num_seqs+1]
+ * host arrays. h_items: host output with room for `capacity` items; the
+ * number needed is sum over b of ceil(Lq_b / 128) <= total_q/128 + num_seqs.
+ * Returns the number of items (>= 0), or PKV_ERR_NULL_POINTER, or
+ * PKV_ERR_BAD_SIZE (num_seqs outside [0, 65535], lengths not monotone or
+ * Lk_b < Lq_b, a sequence of 2^22 or more query rows, or capacity too small).
+ */
+int32_t pkv_prefill_plan(const int32_t* h_cu_seqlens_q, const int32_t* h_cu_seqlens_k, int32_t num_seqs,
+                         int32_t* h_items, int32_t capacity);
 
 /*
  * pkv_decode -- single-query GQA decode attention over the paged cache, the

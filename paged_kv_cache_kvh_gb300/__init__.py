@@ -20,6 +20,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 from . import metadata  # noqa: F401  (host index preparation)
@@ -50,6 +51,7 @@ _SIGNATURES = {
                                           _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
                                           _vp]),
     "pkv_prefill_workspace_bytes": (_sz, [_i32, _i32, _i32]),
+    "pkv_prefill_plan": (_i32, [_vp, _vp, _i32, _vp, _i32]),
     "pkv_decode": (ctypes.c_int, [_vp, _i64, _vp, _vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                   _f32, _vp, _vp, _sz, _vp]),
     "pkv_decode_workspace_bytes": (_sz, [_i32, _i32, _i32]),
@@ -186,25 +188,58 @@ def _prefill(entry, dtype, q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seql
         _ptr(k_cache) if block_tables is not None else None, _ptr(v_cache) if block_tables is not None else None,
         num_blocks, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k),
         _ptr(block_tables), bt_stride, num_seqs, NUM_HEADS, NUM_KV_HEADS, HEAD_DIM, BLOCK_SIZE,
-        float(softmax_scale), _ptr(out), _ptr(workspace), 0 if workspace is None else workspace.numel(),
-        _stream(stream)), entry)
+        float(softmax_scale), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(stream)), entry)
     return out
 
 
+def pkv_prefill_plan(cu_seqlens_q, cu_seqlens_k, device="cuda"):
+    """Tile plan for pkv_prefill_varlen(_f16) from host cu_seqlens (numpy,
+    lists or CPU tensors): the (query tile, sequence) items that hold rows,
+    longest key range first, as an int32 tensor on `device` (numpy if None).
+    Built once per step and passed as plan= to every layer's prefill."""
+    cq = np.ascontiguousarray(np.asarray(cu_seqlens_q.cpu() if torch.is_tensor(cu_seqlens_q) else cu_seqlens_q,
+                                         dtype=np.int32))
+    ck = np.ascontiguousarray(np.asarray(cu_seqlens_k.cpu() if torch.is_tensor(cu_seqlens_k) else cu_seqlens_k,
+                                         dtype=np.int32))
+    num_seqs = cq.size - 1
+    _need(num_seqs >= 0 and ck.size == num_seqs + 1, "cu_seqlens sizes")
+    cap = int(cq[-1] - cq[0]) // 128 + num_seqs + 1 if num_seqs > 0 else 1
+    items = np.empty(cap, dtype=np.int32)
+    n = int(_lib.pkv_prefill_plan(cq.ctypes.data, ck.ctypes.data, num_seqs, items.ctypes.data, cap))
+    if n < 0:
+        raise PkvError(n, "pkv_prefill_plan")
+    items = items[:n].copy()
+    return items if device is None else torch.from_numpy(items).to(device)
+
+
+def _plan_arg(plan, workspace):
+    if plan is None:
+        return workspace
+    _need(workspace is None, "pass either plan or workspace")
+    _need(torch.is_tensor(plan) and plan.is_cuda and plan.dtype == torch.int32 and plan.is_contiguous(),
+          "plan must be a contiguous int32 CUDA tensor (pkv_prefill_plan)")
+    return plan if plan.numel() > 0 else None
+
+
 def pkv_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, *, k=None, v=None,
-                       k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None, stream=None):
+                       k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None, plan=None,
+                       stream=None):
     """flash_attn_varlen_func(q, k, v, ..., causal=True, block_table=block_tables).
 
     Paged keys (k_cache/v_cache through block_tables) when block_tables is
-    given, else contiguous k/v. Returns out [total_q, 16, 128] bf16."""
+    given, else contiguous k/v. plan: optional tile plan (pkv_prefill_plan of
+    the same cu_seqlens). Returns out [total_q, 16, 128] bf16."""
+    workspace = _plan_arg(plan, workspace)
     return _prefill("pkv_prefill_varlen", torch.bfloat16, q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
                     softmax_scale, k, v, k_cache, v_cache, block_tables, out, workspace, stream)
 
 
 def pkv_prefill_varlen_f16(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, softmax_scale, *, k=None,
                            v=None, k_cache=None, v_cache=None, block_tables=None, out=None, workspace=None,
-                           stream=None):
+                           plan=None, stream=None):
     """pkv_prefill_varlen on fp16 tensors; returns fp16."""
+    workspace = _plan_arg(plan, workspace)
     return _prefill("pkv_prefill_varlen_f16", torch.float16, q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
                     max_seqlen_k, softmax_scale, k, v, k_cache, v_cache, block_tables, out, workspace, stream)
 

@@ -5,7 +5,9 @@
 // element stride, heads contiguous, cache rows of num_kv_heads*head_dim,
 // one slot per token) plus the limits of these kernels; a failed check
 // returns an error code before anything is launched.
+#include <algorithm>
 #include <cstdio>
+#include <vector>
 
 #include "pkv_common.cuh"
 
@@ -30,7 +32,8 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
                            int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
                            int32_t num_blocks, const int32_t* cu_q, const int32_t* cu_k, int32_t max_seqlen_q,
                            int32_t max_seqlen_k, const int32_t* block_tables, int32_t bt_stride, int32_t num_seqs,
-                           float scale, void* out, unsigned int* err, cudaStream_t stream, Elem elem);
+                           float scale, const int32_t* items, int32_t num_items, void* out, unsigned int* err,
+                           cudaStream_t stream, Elem elem);
 size_t prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32_t num_heads);
 cudaError_t launch_prefill_metadata(const int32_t* num_cached, const int32_t* num_scheduled,
                                     const int32_t* block_tables, int32_t bt_stride, int32_t num_blocks,
@@ -141,6 +144,31 @@ size_t pkv_prefill_workspace_bytes(int32_t num_seqs, int32_t max_seqlen_q, int32
   return pkv::prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads);
 }
 
+int32_t pkv_prefill_plan(const int32_t* h_cu_seqlens_q, const int32_t* h_cu_seqlens_k, int32_t num_seqs,
+                         int32_t* h_items, int32_t capacity) {
+  if (!h_cu_seqlens_q || !h_cu_seqlens_k || (!h_items && capacity > 0)) return PKV_ERR_NULL_POINTER;
+  if (num_seqs < 0 || num_seqs > 65535 || capacity < 0) return PKV_ERR_BAD_SIZE;
+  struct Item {
+    int32_t code;     // (qt << 16) | b
+    int32_t n_tiles;  // 128-key tiles the query tile attends to
+  };
+  std::vector<Item> v;
+  for (int32_t b = 0; b < num_seqs; ++b) {
+    const int64_t lq = static_cast<int64_t>(h_cu_seqlens_q[b + 1]) - h_cu_seqlens_q[b];
+    const int64_t lk = static_cast<int64_t>(h_cu_seqlens_k[b + 1]) - h_cu_seqlens_k[b];
+    if (lq < 0 || lk < lq || lq >= (int64_t{1} << 22)) return PKV_ERR_BAD_SIZE;
+    for (int64_t qt = (lq + 127) / 128 - 1; qt >= 0; --qt) {
+      const int64_t last_pos = lk - lq + std::min<int64_t>(lq - 1, qt * 128 + 127);
+      v.push_back({static_cast<int32_t>((qt << 16) | b), static_cast<int32_t>(last_pos / 128 + 1)});
+    }
+  }
+  if (v.size() > static_cast<size_t>(capacity)) return PKV_ERR_BAD_SIZE;
+  // most key tiles first; ties by lower sequence, then higher query tile (the build order)
+  std::stable_sort(v.begin(), v.end(), [](const Item& x, const Item& y) { return x.n_tiles > y.n_tiles; });
+  for (size_t i = 0; i < v.size(); ++i) h_items[i] = v[i].code;
+  return static_cast<int32_t>(v.size());
+}
+
 size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t max_context_len) {
   (void)num_heads;
   if (num_seqs <= 0 || max_context_len <= 0) return 0;
@@ -179,15 +207,22 @@ int prefill_common(const void* q, int64_t q_row_stride, int32_t total_q, const v
     if (kv_row_stride < kvrow) return PKV_ERR_BAD_STRIDE;
     if (!aligned16(k) || !aligned16(v) || (kv_row_stride % 8) != 0) return PKV_ERR_ALIGNMENT;
   }
-  const size_t need = pkv::prefill_workspace_bytes(num_seqs, max_seqlen_q, num_heads);
-  if (need > 0 && (!workspace || workspace_bytes < need)) return PKV_ERR_WORKSPACE;
+  // The prefill needs no workspace; one passed is a tile plan (pkv_prefill_plan).
+  const int32_t* items = nullptr;
+  int32_t num_items = 0;
+  if (workspace && workspace_bytes > 0) {
+    if (workspace_bytes % 4 != 0 || workspace_bytes / 4 > (size_t{1} << 28)) return PKV_ERR_BAD_SIZE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 4 != 0) return PKV_ERR_ALIGNMENT;
+    items = static_cast<const int32_t*>(workspace);
+    num_items = static_cast<int32_t>(workspace_bytes / 4);
+  }
   unsigned int* err = nullptr;
   st = error_word(&err);
   if (st != PKV_OK) return st;
   return launched(pkv::launch_prefill(q, q_row_stride, total_q, k, v, kv_row_stride, total_k, k_cache, v_cache,
                                       num_blocks, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
-                                      block_tables, block_table_stride, num_seqs, softmax_scale, out, err, stream,
-                                      elem));
+                                      block_tables, block_table_stride, num_seqs, softmax_scale, items, num_items,
+                                      out, err, stream, elem));
 }
 
 int decode_common(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache, int32_t num_blocks,

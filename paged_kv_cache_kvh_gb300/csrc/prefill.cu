@@ -88,6 +88,7 @@ struct PrefillParams {
   int32_t paged;
   float scale_log2;
   int32_t ahead;  // block index distance to the CTA likely to run next on this SM (the SM count)
+  const int32_t* items;  // optional tile plan: (qt << 16) | b per item, CTA = 8 * item + hk; NULL: all pairs
   uint16_t* out;  // 16-bit elements of the call's type
   unsigned int* err;
 };
@@ -152,11 +153,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   // ---- work item: (query tile, sequence, kv head), longest tiles first ----
+  // Without a plan the grid covers every (query tile, sequence) pair, query
+  // tiles in descending order; with one, CTA 8i + hk takes the plan's item i.
   const int per_tile = p.num_seqs * kHkv;
-  const int qt = p.max_q_tiles - 1 - static_cast<int>(blockIdx.x) / per_tile;
-  const int rem = static_cast<int>(blockIdx.x) % per_tile;
-  const int b = rem / kHkv;
-  const int hk = rem % kHkv;
+  auto item_of = [&](int cta, int& qt_, int& b_, int& hk_) {
+    hk_ = cta % kHkv;
+    if (p.items) {
+      const int code = p.items[cta / kHkv];
+      qt_ = code >> 16;
+      b_ = code & 0xffff;
+    } else {
+      qt_ = p.max_q_tiles - 1 - cta / per_tile;
+      b_ = (cta % per_tile) / kHkv;
+    }
+  };
+  int qt, b, hk;
+  item_of(static_cast<int>(blockIdx.x), qt, b, hk);
+  if (b >= p.num_seqs || qt < 0) {  // a plan for other cu_seqlens: skip the item
+    if (threadIdx.x == 0) flag_error(p.err, PKV_DEVERR_BAD_SEQLEN);
+    return;
+  }
 
   const int cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1];
   const int ck0 = p.cu_k[b], ck1 = p.cu_k[b + 1];
@@ -245,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // usually in L2 already).
       const int nb = static_cast<int>(blockIdx.x) + p.ahead;
       if (nb < static_cast<int>(gridDim.x)) {
-        const int qt2 = p.max_q_tiles - 1 - nb / per_tile;
-        const int b2 = (nb % per_tile) / kHkv, hk2 = (nb % per_tile) % kHkv;
-        const int q0 = p.cu_q[b2], q1 = p.cu_q[b2 + 1];
+        int qt2, b2, hk2;
+        item_of(nb, qt2, b2, hk2);
+        const int q0 = b2 < p.num_seqs ? p.cu_q[b2] : 0, q1 = b2 < p.num_seqs ? p.cu_q[b2 + 1] : 0;
         if (qt2 * kBM < q1 - q0) {
           for (int g = 0; g < kGroup; ++g) {
             tma_prefetch_l2_3d(&tm_q, 0, kGroup * hk2 + g, q0 + qt2 * kBM);
@@ -594,7 +610,8 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
                            int64_t kv_row_stride, int32_t total_k, const void* k_cache, const void* v_cache,
                            int32_t num_blocks, const int32_t* cu_q, const int32_t* cu_k, int32_t max_seqlen_q,
                            int32_t max_seqlen_k, const int32_t* block_tables, int32_t bt_stride, int32_t num_seqs,
-                           float scale, void* out, unsigned int* err, cudaStream_t stream, Elem elem) {
+                           float scale, const int32_t* items, int32_t num_items, void* out, unsigned int* err,
+                           cudaStream_t stream, Elem elem) {
   if (num_seqs == 0 || max_seqlen_q == 0 || total_q == 0) return cudaSuccess;
   CUtensorMap tq, tk, tv;
   const bool paged = block_tables != nullptr;
@@ -630,9 +647,11 @@ cudaError_t launch_prefill(const void* q, int64_t q_row_stride, int32_t total_q,
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
     p.ahead = sms;
   }
+  p.items = num_items > 0 ? items : nullptr;
   p.out = static_cast<uint16_t*>(out);
   p.err = err;
-  const int64_t nblocks = static_cast<int64_t>(p.max_q_tiles) * num_seqs * kHkv;
+  const int64_t nblocks = p.items ? static_cast<int64_t>(num_items) * kHkv
+                                  : static_cast<int64_t>(p.max_q_tiles) * num_seqs * kHkv;
   if (nblocks > 0x7fffffff) return cudaErrorInvalidValue;
   const unsigned nb = static_cast<unsigned>(nblocks);
   return elem == Elem::kF16 ? launch_typed<Elem::kF16>(tq, tk, tv, p, nb, stream)

@@ -275,3 +275,54 @@ def test_chunked_prefill_full_size(pkv):
     19 chunks starting mid-block): every call in order, sampled rows."""
     wl = W.chunked_prefill()
     _run_calls(pkv, wl.seqs, wl.num_blocks, seed=wl.seed, rng=np.random.default_rng(6), per_seq=3)
+
+
+@pytest.mark.parametrize("specs", [[(0, 300), (0, 77), (0, 1000)], [(1024, 64), (256, 500), (0, 129)],
+                                   [(5000, 300), (37, 900)], [(0, 1)]])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_plan_gives_identical_output(pkv, specs, dtype):
+    """A host tile plan (pkv_prefill_plan) launches only the query tiles that
+    hold rows, longest first; the output is bit-identical to the plain grid's."""
+    dev = "cuda"
+    rng = np.random.default_rng(len(specs))
+    seqs, nb = _seqs_with_tables(specs, rng)
+    gen = W.make_generator(31, dev)
+    kc, vc = pool_tensors(nb, gen, dev, dtype)
+    T = sum(s.num_scheduled_tokens for s in seqs)
+    _, q, k, v = W.fused_qkv(T, gen, dev, dtype=dtype)
+    meta = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
+    prefill = pkv.pkv_prefill_varlen_f16 if dtype == torch.float16 else pkv.pkv_prefill_varlen
+    cu_q, cu_k, bt = to_dev(meta["cu_seqlens_q"], dev), to_dev(meta["cu_seqlens_k"], dev), to_dev(meta["block_tables"], dev)
+    pkv.pkv_store_kvcache(k, v, kc, vc, to_dev(meta["slot_mapping"], dev))
+    plan = pkv.pkv_prefill_plan(meta["cu_seqlens_q"], meta["cu_seqlens_k"])
+    assert plan.numel() == sum((s.num_scheduled_tokens + 127) // 128 for s in seqs)
+    args = (q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE)
+    a = prefill(*args, k_cache=kc, v_cache=vc, block_tables=bt)
+    b = prefill(*args, k_cache=kc, v_cache=vc, block_tables=bt, plan=plan)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error() == 0
+    assert torch.equal(a, b)
+
+
+def test_plan_naming_missing_sequences_is_flagged(pkv):
+    """A plan built for more sequences than the call has is skipped where it
+    names a missing sequence (flagged), never dereferenced."""
+    dev = "cuda"
+    rng = np.random.default_rng(3)
+    seqs, nb = _seqs_with_tables([(0, 200)], rng)
+    gen = W.make_generator(32, dev)
+    kc, vc = pool_tensors(nb, gen, dev)
+    _, q, k, v = W.fused_qkv(200, gen, dev)
+    meta = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
+    pkv.pkv_store_kvcache(k, v, kc, vc, to_dev(meta["slot_mapping"], dev))
+    plan = pkv.pkv_prefill_plan([0, 200, 400], [0, 200, 400])   # two sequences
+    out = pkv.pkv_prefill_varlen(q, to_dev(meta["cu_seqlens_q"], dev), to_dev(meta["cu_seqlens_k"], dev),
+                                 meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc,
+                                 block_tables=to_dev(meta["block_tables"], dev), plan=plan)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_error(clear=True) & pkv.PKV_DEVERR_BAD_SEQLEN
+    ref = pkv.pkv_prefill_varlen(q, to_dev(meta["cu_seqlens_q"], dev), to_dev(meta["cu_seqlens_k"], dev),
+                                 meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc,
+                                 block_tables=to_dev(meta["block_tables"], dev))
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)          # the one real sequence is complete
