@@ -232,7 +232,7 @@ def run_ours(args, rank, world, dev):
         raise RuntimeError(f"device error word {err:#x} after the timed region")
 
     # ---- e2e: host buffers through the C ABI ----
-    e2e = run_e2e(pkv, c, args, dev)
+    e2e = run_e2e(pkv, c, args, dev, world)
 
     hbm, bf16, bf16_sus, src = _peaks()
     ach = c["decode_alg_bytes"] / (dec_ms * 1e-3) / 1e9
@@ -266,11 +266,13 @@ def run_ours(args, rank, world, dev):
     return res
 
 
-def run_e2e(pkv, c, args, dev):
+def run_e2e(pkv, c, args, dev, world=1):
     """Store + decode from pinned host buffers: every step copies its inputs
     host-to-device and reads its output back. Two device input/output sets and
     separate copy streams let step k+1's copies overlap step k's kernels (the
-    way a serving loop would issue them); each step still moves all its bytes."""
+    way a serving loop would issue them); each step still moves all its bytes.
+    With several ranks the value is the whole job's, like the headline's:
+    all ranks' bytes over the slowest rank's time, barriers on both sides."""
     B = c["B"]
     hq = c["q"].contiguous().cpu().pin_memory()
     hk = c["k"].contiguous().cpu().pin_memory()
@@ -311,6 +313,8 @@ def run_e2e(pkv, c, args, dev):
     for k in range(max(3, args.warmup)):
         step(k)
     torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(comp)
     h2d.wait_event(a)
@@ -320,11 +324,13 @@ def run_e2e(pkv, c, args, dev):
     comp.wait_stream(d2h)
     b.record(comp)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    ms = max_over_ranks(a.elapsed_time(b), world, dev) / args.steps
     if not torch.equal(hout[(args.steps - 1) % 2], c["out"].cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident step")
     h2d_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hslot, hctx, hbt))
-    return {"value": round(c["kv_bytes"] / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
+    return {"value": round(job_throughput(c["kv_bytes"], world, ms) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 5),
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": hout[0].numel() * hout[0].element_size(),
             "pipelining": "inputs and outputs double-buffered; copies on their own streams overlap the previous "
                           "step's kernels"}
