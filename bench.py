@@ -252,6 +252,8 @@ def run_ours(args, rank, world, dev):
                       "l2": "inputs larger than L2 (2.4 GB of live K/V read per step)",
                       "parallelism": f"replicas x{world}"},
            "roofline": roof, "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clocks}
+    if rank == 0:
+        res["fused_step"] = run_fused_step(pkv, c, args)
     if rank == 0 and not args.no_prefill:
         res["prefill"] = run_prefill(pkv, args, dev, bf16)
     if rank == 0:
@@ -264,6 +266,30 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(c, budget_s=args.cpu_seconds)
     return res
+
+
+def run_fused_step(pkv, c, args):
+    """The headline batch's store + decode as one launch (pkv_store_decode, the
+    new token's K/V written by the CTA that streams its block), device-resident
+    inputs, CUDA events around `steps` back-to-back steps."""
+    def step():
+        pkv.pkv_store_decode(c["q"], c["k"], c["v"], c["slot"], c["kc"], c["vc"], c["bt"], c["ctx"],
+                             W.MAX_MODEL_LEN, W.SCALE, c["ws"], out=c["out"])
+
+    for _ in range(args.warmup):
+        step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    if pkv.pkv_device_error():
+        raise RuntimeError("device error word set by the fused step")
+    ms = a.elapsed_time(b) / args.steps
+    return {"ms_per_step": round(ms, 5), "kv_gbs": round(c["kv_bytes"] / (ms * 1e-3) / 1e9, 1),
+            "gpu_launches_per_step": 1, "note": "same batch and bytes as the headline step, one launch"}
 
 
 def run_e2e(pkv, c, args, dev, world=1):
