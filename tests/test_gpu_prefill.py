@@ -72,9 +72,14 @@ def _run(pkv, seqs, nb, seed, *, poison=False, sample_rows=None, check_contiguou
     pkv.pkv_store_kvcache(k, v, kc, vc, slot)
     out = prefill(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE,
                   k_cache=kc, v_cache=vc, block_tables=bt)
+    # the same call through a host tile plan launches only the tiles with rows: identical bits
+    plan = pkv.pkv_prefill_plan(meta["cu_seqlens_q"], meta["cu_seqlens_k"], dev)
+    out_planned = prefill(q, cu_q, cu_k, meta["max_seqlen_q"], meta["max_seqlen_k"], W.SCALE,
+                          k_cache=kc, v_cache=vc, block_tables=bt, plan=plan)
     torch.cuda.synchronize()
     assert pkv.pkv_device_error() == 0
     assert out.dtype == dtype
+    assert torch.equal(out, out_planned)
 
     om = oracle.prepare_prefill(host.seqs, W.BLOCK_SIZE)
     ks, vs = host.slots()
