@@ -271,23 +271,27 @@ size_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t m
  * users of this library, not for the method.
  *
  * Who needs it: an engine that sized its KV-cache pool to take all device
- * memory left after start-up (nano-vLLM does exactly this), a plug-in whose
- * host process owns the only device allocator, or a latency-critical loop
- * that must not call cudaMalloc because it can synchronise the device. None
- * of them can hand pkv_decode a workspace.
+ * memory left after start-up, a plug-in whose host process owns the only
+ * device allocator, or a latency-critical loop that must not call cudaMalloc
+ * because it can synchronise the device. None of them can hand pkv_decode a
+ * workspace.
  *
- * Same arguments and result as pkv_decode, without the workspace: the
- * split-KV scratch lives in a fixed array of PKV_DECODE_NOALLOC_SCRATCH_BYTES
- * that is part of the library's device image, reserved on every GPU that
- * loads the library and held until the process exits. The call allocates
- * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ * Same arguments and result as pkv_decode (bf16 only; there is no fp16 form),
+ * without the workspace: the split-KV scratch lives in a fixed array of
+ * PKV_DECODE_NOALLOC_SCRATCH_BYTES that is part of the library's device
+ * image, reserved on every GPU that loads the library and held until the
+ * process exits. The call allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library routine).
  *   - Limit: sizes with pkv_decode_workspace_bytes(num_seqs, num_heads,
  *     max_context_len) > PKV_DECODE_NOALLOC_SCRATCH_BYTES are rejected with
  *     PKV_ERR_SCRATCH_LIMIT before anything is launched (e.g. 256 sequences
- *     with max_context_len 4096 fit; 512 sequences fit up to 2048).
- *   - The first call on each device, with that device current, looks up the
- *     array's device address (cudaGetSymbolAddress) and caches it; make that
- *     first call before any stream capture.
+ *     with max_context_len 4096 fit; 512 sequences fit up to 2048). Every
+ *     other argument error pkv_decode reports is reported too, also before
+ *     anything is queued on the stream.
+ *   - The call passes the kernel the array's device address, which it asks
+ *     the runtime for (cudaGetSymbolAddress) with the calling thread's device
+ *     current, and caches per device and context. The first call on each
+ *     device makes that lookup: make it before any stream capture.
  *   - Every call shares the one array and leaves its contents behind; each
  *     call first clears (cudaMemsetAsync on `stream`) the part that must start
  *     at zero. Calls whose execution overlaps on the GPU (different streams

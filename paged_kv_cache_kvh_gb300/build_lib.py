@@ -7,6 +7,7 @@ Output: ``paged_kv_cache_kvh_gb300/libpkv.so`` (git-ignored).
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
 import shutil
 import subprocess
@@ -41,7 +42,8 @@ def build(force: bool = False, extra_flags=(), out: str = LIB, verbose: bool = F
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     headers.append(os.path.join(ROOT, "include", "pkv.h"))
-    tag = "x" + str(abs(hash(tuple(extra_flags))) % 100000) if extra_flags else ""
+    # objects built with extra flags get a tag that is stable across processes
+    tag = "x" + hashlib.sha256("\0".join(extra_flags).encode()).hexdigest()[:10] if extra_flags else ""
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)

@@ -14,36 +14,19 @@
 // The array has no device address known to host code until it is looked up:
 // in host code its name only stands for a host-side shadow symbol, and handing
 // that to a kernel would fault or, where the GPU can reach host memory,
-// silently touch the wrong memory. So the first call on each device (with that
-// device current) asks the runtime for the real address with
-// cudaGetSymbolAddress, checks the result, caches it per device, and every
-// call passes that address on to the kernel.
+// silently touch the wrong memory. So every call asks the runtime for the real
+// address (cudaGetSymbolAddress, with the calling thread's device current),
+// checks the result and passes that address on to the kernel. The address is
+// cached per device and context and looked up again when the context changes
+// (a cudaDeviceReset moves the array). The first call on a device is the one
+// that makes the lookup, and it may load the library's device code there:
+// make that first call before any stream capture.
 #include "pkv_common.cuh"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 // The scratch itself: PKV_DECODE_NOALLOC_SCRATCH_BYTES bytes per device.
 static __device__ __align__(256) unsigned char g_decode_noalloc_scratch[PKV_DECODE_NOALLOC_SCRATCH_BYTES];
-
-void* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of this device's scratch array (looked up once per device).
-int scratch_address(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_decode_noalloc_scratch) != cudaSuccess || p == nullptr) {
-      (void)cudaGetLastError();
-      return PKV_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return PKV_OK;
-}
 
 }  // namespace
 
@@ -56,8 +39,17 @@ extern "C" int pkv_decode_noalloc(const void* q, int64_t q_row_stride, const voi
   if (num_seqs == 0) return PKV_OK;
   const size_t need = pkv_decode_workspace_bytes(num_seqs, num_heads, max_context_len);
   if (need > static_cast<size_t>(PKV_DECODE_NOALLOC_SCRATCH_BYTES)) return PKV_ERR_SCRATCH_LIMIT;
+  // Everything pkv_decode would reject is rejected here first, so a refused
+  // call leaves nothing queued on the stream.
+  unsigned int* err = nullptr;
+  int st = pkv::device_error_word(&err);
+  if (st != PKV_OK) return st;
   void* scratch = nullptr;
-  int st = scratch_address(&scratch);
+  st = pkv::symbol_address(&g_decode_noalloc_scratch, pkv::kSymbolDecodeScratch, &scratch);
+  if (st != PKV_OK) return st;
+  st = pkv::check_decode_args(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                              context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                              softmax_scale, out, scratch, static_cast<size_t>(PKV_DECODE_NOALLOC_SCRATCH_BYTES));
   if (st != PKV_OK) return st;
   // The split-KV tickets at the start of the scratch must start at zero. The
   // array keeps whatever the previous call left, so clear them on the stream.

@@ -5,8 +5,11 @@
 // element stride, heads contiguous, cache rows of num_kv_heads*head_dim,
 // one slot per token) plus the limits of these kernels; a failed check
 // returns an error code before anything is launched.
+#include <cuda.h>  // driver types for the context-id query (resolved at run time, no libcuda link)
+
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 #include <vector>
 
 #include "pkv_common.cuh"
@@ -52,7 +55,47 @@ constexpr int kMaxDevices = 64;
 // Per-device error word: OR of PKV_DEVERR_* bits raised by any kernel.
 __device__ unsigned int g_pkv_error_word;
 
-unsigned int* g_err_ptr[kMaxDevices] = {nullptr};
+// Cached device addresses of the library's __device__ variables, keyed by the
+// id of the context they were looked up in. Host threads share it under a lock.
+constexpr int kNumSymbols = 2;
+struct SymbolSlot {
+  bool valid = false;
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
+std::mutex g_symbol_lock;
+SymbolSlot g_symbols[kMaxDevices][kNumSymbols];
+std::once_flag g_cc_once[kMaxDevices];
+int g_cc_ok[kMaxDevices] = {0};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (cuCtxGetId; ids are never
+// reused), through driver entry points the runtime hands out. False when
+// there is no current context yet or the driver lacks the query.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+    (void)cudaGetLastError();
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* err) {
   __shared__ __align__(8) uint64_t never;
@@ -65,22 +108,7 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, unsigned int* err) {
   if (threadIdx.x == 0) pkv::mbar_wait(bar, 0, err, limit_ns);
 }
 
-// Address of this device's error word (looked up once per device).
-int error_word(unsigned int** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PKV_ERR_CUDA;
-  if (!g_err_ptr[dev]) {
-    int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    if (major != 10 || minor != 3) return PKV_ERR_DEVICE;
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_pkv_error_word) != cudaSuccess) return PKV_ERR_CUDA;
-    g_err_ptr[dev] = static_cast<unsigned int*>(p);
-  }
-  *out = g_err_ptr[dev];
-  return PKV_OK;
-}
+int error_word(unsigned int** out) { return pkv::device_error_word(out); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -100,6 +128,85 @@ int check_attention_shape(int32_t num_heads, int32_t num_kv_heads, int32_t head_
 }
 
 }  // namespace
+
+namespace pkv {
+
+int symbol_address(const void* symbol, int slot, void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kNumSymbols) {
+    (void)cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
+  if (have_id) {
+    std::lock_guard<std::mutex> lock(g_symbol_lock);
+    const SymbolSlot& s = g_symbols[dev][slot];
+    if (s.valid && s.ctx_id == id) {
+      *out = s.addr;
+      return PKV_OK;
+    }
+  }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || p == nullptr) {
+    (void)cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  if (!have_id) have_id = current_context_id(&id);  // the lookup made the context current
+  if (have_id) {
+    std::lock_guard<std::mutex> lock(g_symbol_lock);
+    g_symbols[dev][slot] = SymbolSlot{true, id, p};
+  }
+  *out = p;
+  return PKV_OK;
+}
+
+int device_error_word(unsigned int** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  std::call_once(g_cc_once[dev], [dev] {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    (void)cudaGetLastError();
+    g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  });
+  if (g_cc_ok[dev] != 1) return PKV_ERR_DEVICE;
+  void* p = nullptr;
+  const int st = symbol_address(&g_pkv_error_word, kSymbolErrorWord, &p);
+  if (st != PKV_OK) return st;
+  *out = static_cast<unsigned int*>(p);
+  return PKV_OK;
+}
+
+int check_decode_args(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                      int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                      const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale,
+                      const void* out, const void* workspace, size_t workspace_bytes) {
+  int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || num_seqs > 65535 || num_blocks < 0 || block_table_stride < 0 || max_context_len < 0 ||
+      max_context_len > (1 << 24))
+    return PKV_ERR_BAD_SIZE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!(softmax_scale > 0.f)) return PKV_ERR_BAD_SIZE;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_NULL_POINTER;
+  if (q_row_stride < static_cast<int64_t>(num_heads) * head_dim) return PKV_ERR_BAD_STRIDE;
+  if (!aligned16(q) || (q_row_stride % 8) != 0 || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PKV_ERR_ALIGNMENT;
+  if (max_context_len > 0) {
+    const size_t need = decode_workspace_bytes(num_seqs, max_context_len);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGNMENT;
+  }
+  return PKV_OK;
+}
+
+}  // namespace pkv
 
 extern "C" {
 
@@ -230,22 +337,10 @@ int decode_common(const void* q, int64_t q_row_stride, const void* k_cache, cons
                   int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                   int32_t max_context_len, float softmax_scale, void* out, void* workspace, size_t workspace_bytes,
                   cudaStream_t stream, const pkv::FusedStore* fused, pkv::Elem elem) {
-  int st = check_attention_shape(num_heads, num_kv_heads, head_dim, block_size);
-  if (st != PKV_OK) return st;
-  if (num_seqs < 0 || num_seqs > 65535 || num_blocks < 0 || block_table_stride < 0 || max_context_len < 0 ||
-      max_context_len > (1 << 24))
-    return PKV_ERR_BAD_SIZE;
-  if (num_seqs == 0) return PKV_OK;
-  if (!(softmax_scale > 0.f)) return PKV_ERR_BAD_SIZE;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out) return PKV_ERR_NULL_POINTER;
-  if (q_row_stride < static_cast<int64_t>(num_heads) * head_dim) return PKV_ERR_BAD_STRIDE;
-  if (!aligned16(q) || (q_row_stride % 8) != 0 || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return PKV_ERR_ALIGNMENT;
-  if (max_context_len > 0) {
-    const size_t need = pkv::decode_workspace_bytes(num_seqs, max_context_len);
-    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return PKV_ERR_ALIGNMENT;
-  }
+  int st = pkv::check_decode_args(q, q_row_stride, k_cache, v_cache, num_blocks, block_tables, block_table_stride,
+                                  context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                  max_context_len, softmax_scale, out, workspace, workspace_bytes);
+  if (st != PKV_OK || num_seqs == 0) return st;
   unsigned int* err = nullptr;
   st = error_word(&err);
   if (st != PKV_OK) return st;

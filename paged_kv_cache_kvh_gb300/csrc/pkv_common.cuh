@@ -306,4 +306,25 @@ struct ElemOps<Elem::kF16> {
   }
 };
 
+// ---- host helpers shared by the entry points (defined in pkv_abi.cu) ----
+
+// Device address of one of this library's __device__ variables in the
+// current context. `slot` names the variable (kSymbol*). The address is cached
+// per device and looked up again whenever the current context changes (a
+// cudaDeviceReset makes a new primary context, and the variable moves).
+constexpr int kSymbolErrorWord = 0;
+constexpr int kSymbolDecodeScratch = 1;
+int symbol_address(const void* symbol, int slot, void** out);
+
+// This device's error word, after checking that the device is sm_103.
+int device_error_word(unsigned int** out);
+
+// The host-side argument checks of pkv_decode / pkv_decode_f16 (shape, sizes,
+// pointers, strides, alignment, workspace), without launching anything.
+int check_decode_args(const void* q, int64_t q_row_stride, const void* k_cache, const void* v_cache,
+                      int32_t num_blocks, const int32_t* block_tables, int32_t block_table_stride,
+                      const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_context_len, float softmax_scale,
+                      const void* out, const void* workspace, size_t workspace_bytes);
+
 }  // namespace pkv

@@ -88,3 +88,34 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(pkv):
     assert e.value.status == pkv.PKV_ERR_SCRATCH_LIMIT
     torch.cuda.synchronize()
     assert torch.all(out == 0)                 # nothing was launched
+
+
+def test_noalloc_zero_sizes_and_rejections_match_decode(pkv):
+    """Empty and all-padding calls, and argument errors: the same outcome as
+    pkv_decode, and a refused call leaves the output untouched."""
+    dev = "cuda"
+    lib = pkv._lib
+    # no sequences: nothing to do
+    assert lib.pkv_decode_noalloc(None, 2048, None, None, 0, None, 16, None, 0, 16, 8, 128, 256, 4096, 0.1,
+                                  None, None) == 0
+    # every row a padding row and max_context_len 0: zeros, no device error
+    q, kc, vc, bt, _ = _case(pkv, 33, [5, 9], dev)
+    ctx0 = torch.zeros(2, dtype=torch.int32, device=dev)
+    out = torch.full_like(q, float("nan"))
+    pkv.pkv_decode_noalloc(q, kc, vc, bt, ctx0, 0, W.SCALE, out)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0)
+    assert pkv.pkv_device_error() == 0
+    # argument errors: pkv_decode's status, and nothing written
+    ws = pkv.decode_workspace(2, W.MAX_MODEL_LEN, dev)
+    out = torch.full_like(q, 7.0)
+    common = [q.data_ptr(), q.stride(0), kc.data_ptr(), vc.data_ptr(), kc.shape[0], bt.data_ptr(), bt.shape[1],
+              ctx0.data_ptr(), 2]
+    for heads, scale, out_ptr in ((32, W.SCALE, out.data_ptr()), (16, -1.0, out.data_ptr()),
+                                  (16, W.SCALE, out.data_ptr() + 2), (16, W.SCALE, None)):
+        tail = [heads, 8, 128, 256, W.MAX_MODEL_LEN, scale, out_ptr]
+        want = lib.pkv_decode(*common, *tail, ws.data_ptr(), ws.numel(), None)
+        got = lib.pkv_decode_noalloc(*common, *tail, None)
+        assert want < 0 and got == want, (heads, scale, want, got)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
