@@ -808,13 +808,14 @@ def ncu_case(kind):
         for _ in range(3):
             pkv.pkv_decode(q, kc, vc, bt, ctx, W.MAX_MODEL_LEN, W.SCALE, ws)
         units = int(m["context_lens"].astype(np.int64).sum()) * W.HKV * W.HEAD_DIM * 4
-    elif kind in ("prefill", "prefill_prefix", "prefill_chunked"):
+    elif kind in ("prefill", "prefill_prefix", "prefill_chunked", "prefill_chunked_plain"):
         # the workload's first call; for the chunked workload call 9, a full
         # 5000-token chunk continuing 5000 cached tokens (whatever values the
         # seeded pool holds stand in for the keys the earlier call stored)
+        # (prefill_chunked_plain: the same call without a tile plan, one CTA per unit)
         wl = {"prefill": W.varlen_prefill, "prefill_prefix": W.prefix_prefill,
-              "prefill_chunked": W.chunked_prefill}[kind]()
-        seqs = wl.seqs[9 if kind == "prefill_chunked" else 0]
+              "prefill_chunked": W.chunked_prefill, "prefill_chunked_plain": W.chunked_prefill}[kind]()
+        seqs = wl.seqs[9 if kind.startswith("prefill_chunked") else 0]
         gen = W.make_generator(wl.seed, dev)
         shape = (wl.num_blocks, W.BLOCK_SIZE, W.HKV, W.HEAD_DIM)
         kc, vc = W.normal_bf16(shape, gen, dev), W.normal_bf16(shape, gen, dev)
@@ -823,7 +824,8 @@ def ncu_case(kind):
         m = pkv.metadata.prepare_prefill(seqs, W.BLOCK_SIZE, force_block_tables=True)
         d = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
         pkv.pkv_store_kvcache(k, v, kc, vc, d(m["slot_mapping"]))
-        plan = pkv.pkv_prefill_plan(m["cu_seqlens_q"], m["cu_seqlens_k"], dev)
+        plan = None if kind == "prefill_chunked_plain" else pkv.pkv_prefill_plan(m["cu_seqlens_q"],
+                                                                                 m["cu_seqlens_k"], dev)
         for _ in range(3):
             pkv.pkv_prefill_varlen(q, d(m["cu_seqlens_q"]), d(m["cu_seqlens_k"]), m["max_seqlen_q"],
                                    m["max_seqlen_k"], W.SCALE, k_cache=kc, v_cache=vc, block_tables=d(m["block_tables"]),
@@ -968,7 +970,8 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=8)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-f16", action="store_true", help="skip the fp16 entry points' timings")
-    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "prefill_chunked", "store", "sweep"])
+    ap.add_argument("--ncu-case", choices=["decode", "prefill", "prefill_prefix", "prefill_chunked",
+                                           "prefill_chunked_plain", "store", "sweep"])
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.ncu_case:

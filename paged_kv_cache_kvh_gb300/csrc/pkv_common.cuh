@@ -215,6 +215,28 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr, uint32_t
   return d;
 }
 
+// smem_desc_sw128 split in its two 32-bit halves, for issuing many products
+// from one thread with few instructions. The low half is (addr >> 4) | (lbo >>
+// 4) << 16; the high half (sbo = 1024, version, swizzle) is the same for every
+// operand here. Shared-window addresses stay below 256 KB, so adding
+// (offset >> 4) to a low half never carries out of the 14-bit address field:
+// desc_lo(addr, lbo) + (offset >> 4) is the low half for addr + offset.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t smem_addr, uint32_t lbo) {
+  return ((smem_addr >> 4) & 0x3FFFu) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kDescHiSw128 = ((1024u >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+
+// tcgen05.mma kind::f16 from the low halves of the A and B descriptors.
+__device__ __forceinline__ void mma_f16kind_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHiSw128)
+      : "memory");
+}
+
 // Instruction descriptor, kind::f16 with fp32 D. ab_format is the A and B
 // element format (both the same): 0 = fp16, 1 = bf16.
 __host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major, bool b_mn_major,

@@ -308,25 +308,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = wait_or_abort(bar(kBarQ), 0, s_abort, p.err);
       auto slot_of = [](int i) { return i % kKvSlots; };
       auto par_of = [](int i) { return static_cast<uint32_t>((i / kKvSlots) & 1); };
+      // Descriptor low halves: each product below costs two 32-bit adds and
+      // the tcgen05.mma (this one thread issues every product of the CTA).
+      const uint32_t lo_kmaj = desc_lo(sbase, 16), lo_v = desc_lo(sbase, kHalfBytes);
       auto issue_s = [&](int g, int n) {
-        const uint32_t qb = sbase + kOffQ + g * kTileBytes;
-        const uint32_t kb = sbase + kOffKV + slot_of(2 * n) * kTileBytes;
+        const uint32_t qa = lo_kmaj + ((kOffQ + g * kTileBytes) >> 4);
+        const uint32_t kbb = lo_kmaj + (kOffKV >> 4) + slot_of(2 * n) * (kTileBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          mma_f16kind_ss(tmem + g * 128, smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                      idesc_s, ks > 0 ? 1u : 0u);
+          const uint32_t off = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+          mma_f16kind_lo(tmem + g * 128, qa + off, kbb + off, idesc_s, ks > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int g, int n) {
-        const uint32_t pbuf = sbase + kOffP + g * kTileBytes;
-        const uint32_t vb = sbase + kOffKV + slot_of(2 * n + 1) * kTileBytes;
+        const uint32_t pa = lo_kmaj + ((kOffP + g * kTileBytes) >> 4);
+        const uint32_t vbb = lo_v + (kOffKV >> 4) + slot_of(2 * n + 1) * (kTileBytes >> 4);
 #pragma unroll
         for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t aoff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          mma_f16kind_ss(tmem + 256 + g * 128, smem_desc_sw128(pbuf + aoff, 16, 1024),
-                      smem_desc_sw128(vb + ks * 16 * 128, kHalfBytes, 1024), idesc_pv,
-                      (n > 0 || ks > 0) ? 1u : 0u);
+          const uint32_t aoff = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+          mma_f16kind_lo(tmem + 256 + g * 128, pa + aoff, vbb + ((ks * 16 * 128) >> 4), idesc_pv,
+                         (n > 0 || ks > 0) ? 1u : 0u);
         }
       };
       if (ok) ok = wait_or_abort(bar(kBarKvFull + slot_of(0)), par_of(0), s_abort, p.err);
