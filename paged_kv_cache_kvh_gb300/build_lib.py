@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
-SOURCES = ["pkv_abi.cu", "store.cu", "decode.cu", "prefill.cu", "decode_noalloc.cu", "metadata.cu"]
+SOURCES = ["pkv_abi.cu", "store.cu", "decode.cu", "prefill.cu", "prefill_persistent.cu", "decode_noalloc.cu",
+           "metadata.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 
