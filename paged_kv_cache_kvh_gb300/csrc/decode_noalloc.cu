@@ -51,10 +51,11 @@ extern "C" int pkv_decode_noalloc(const void* q, int64_t q_row_stride, const voi
                               context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context_len,
                               softmax_scale, out, scratch, static_cast<size_t>(PKV_DECODE_NOALLOC_SCRATCH_BYTES));
   if (st != PKV_OK) return st;
-  // The split-KV tickets at the start of the scratch must start at zero. The
-  // array keeps whatever the previous call left, so clear them on the stream.
+  // The split-KV tickets and the two work counters after them at the start
+  // of the scratch must start at zero. The array keeps whatever the previous
+  // call left, so clear them on the stream.
   if (need > 0) {
-    const size_t tickets = static_cast<size_t>(num_seqs) * sizeof(int32_t);
+    const size_t tickets = (static_cast<size_t>(num_seqs) + 2) * sizeof(int32_t);
     if (cudaMemsetAsync(scratch, 0, tickets, stream) != cudaSuccess) {
       (void)cudaGetLastError();
       return PKV_ERR_CUDA;
