@@ -162,6 +162,26 @@ def _prequeue(ms):
     torch.cuda._sleep(int(ms * 2.2e6))  # about 2.2e6 SM cycles per ms at the 2.07 GHz maximum clock
 
 
+def _sm_count():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+def _decode_kernel(num_seqs, max_context_len=W.MAX_MODEL_LEN):
+    """The decode kernel the library launches for these sizes (its rule: whole
+    256-token chunks, i.e. num_seqs * ceil(max_ctx / 256) >= 608, and at most
+    512 sequences take the persistent form)."""
+    whole = num_seqs * (-(-max_context_len // W.BLOCK_SIZE)) >= 608
+    return "decode_persistent_kernel" if whole and num_seqs <= 512 else "decode_split_kernel"
+
+
+def _prefill_kernel(num_items, max_seqlen_k):
+    """The prefill kernel the library launches for a planned call (its rule:
+    at least two (item, kv head) units per SM and keys <= 4096)."""
+    persistent = 8 * num_items >= 2 * _sm_count() and max_seqlen_k <= 4096
+    return ("prefill_persistent_kernel", "prefill_persistent.cu") if persistent else ("prefill_tc_kernel",
+                                                                                       "prefill.cu")
+
+
 def max_over_ranks(ms, world, device):
     """Slowest rank's time: every rank does the same work (replicas)."""
     if world <= 1:
@@ -245,7 +265,7 @@ def run_ours(args, rank, world, dev):
 
     hbm, bf16, bf16_sus, src = _peaks()
     ach = c["decode_alg_bytes"] / (dec_ms * 1e-3) / 1e9
-    roof = {"kernel": "decode_split_kernel", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+    roof = {"kernel": _decode_kernel(c["B"]), "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
             "unit": "GB/s", "frac": round(ach / hbm, 4), "peak_source": f"{src} (hbm copy)",
             "alg_bytes_per_launch": c["decode_alg_bytes"], "avg_launch_ms": round(dec_ms, 5),
             "traffic": _traffic("decode.cu", c["kv_bytes"])}
@@ -285,10 +305,10 @@ def run_ours(args, rank, world, dev):
         res["sweep"] = run_sweep(pkv, args, dev, hbm)
         res["padded_graph"] = run_padded_graph(pkv, args, dev, hbm)
         sw, pg = res["sweep"], res["padded_graph"]
-        rooflines.append({"kernel": "decode_split_kernel (store fused)", "workload": "sweep_28l_b512 graph",
+        rooflines.append({"kernel": _decode_kernel(512) + " (store fused)", "workload": "sweep_28l_b512 graph",
                           "dtype": "bf16", "achieved": sw["fused_store_decode"]["kv_gbs"], "peak": hbm,
                           "unit": "GB/s", "frac": sw["fused_store_decode"]["frac_of_hbm"], "traffic": None})
-        rooflines.append({"kernel": "decode_split_kernel", "workload": "padded_b200_in_graph256", "dtype": "bf16",
+        rooflines.append({"kernel": _decode_kernel(256), "workload": "padded_b200_in_graph256", "dtype": "bf16",
                           "achieved": pg["live_kv_gbs"], "peak": hbm, "unit": "GB/s", "frac": pg["frac_of_hbm"],
                           "traffic": None})
     if rank == 0 and not args.no_f16:
@@ -534,6 +554,14 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
                     cl.setdefault("ev", []).append((e0, e1, e2, e3, e4))
         torch.cuda.synchronize()
         flops = sum(cl["flops"] for cl in calls)
+        # which kernel ran each planned call; the workload's roofline names the
+        # one that did most of its FLOPs, its traffic is that kernel's capture
+        by_kernel = {}
+        for cl in calls:
+            kname = _prefill_kernel(cl["plan"].numel(), cl["m"]["max_seqlen_k"])
+            by_kernel[kname] = by_kernel.get(kname, 0) + cl["flops"]
+        kname, kfile = max(by_kernel, key=by_kernel.get)
+        kernels = {k[0]: round(v / flops, 3) for k, v in by_kernel.items()}
         t_pre = sum(ev[1].elapsed_time(ev[2]) for cl in calls for ev in cl["ev"]) / iters
         t_noplan = sum(ev[3].elapsed_time(ev[4]) for cl in calls for ev in cl["ev"]) / iters
         t_st = sum(ev[0].elapsed_time(ev[1]) for cl in calls for ev in cl["ev"]) / iters
@@ -544,13 +572,14 @@ def run_prefill(pkv, args, dev, bf16_peak, dtype=torch.bfloat16):
                      "plan": "host tile plan per call (pkv_prefill_plan), built with the metadata, untimed",
                      "no_plan": {"prefill_ms": round(t_noplan, 4),
                                  "tflops": round(flops / (t_noplan * 1e-3) / 1e12, 1)},
-                     "roofline": {"kernel": "prefill_tc_kernel", "bound": "tensor", "achieved": round(tf, 1),
+                     "kernels_by_flop_share": kernels,
+                     "roofline": {"kernel": kname, "bound": "tensor", "achieved": round(tf, 1),
                                   "peak": bf16_peak, "unit": "TFLOP/s", "frac": round(tf / bf16_peak, 4),
                                   "peak_source": ("measured bf16 dense (cuBLAS burst) x nominal fp16/bf16 ratio 1"
                                                   if f16 else "measured bf16 dense (cuBLAS burst)"),
-                                  "traffic": None if f16 else _traffic("prefill.cu", flops, case=name),
+                                  "traffic": None if f16 else _traffic(kfile, flops, case=name),
                                   "traffic_note": "ncu DRAM bytes of one planned launch: "
-                                                  + str(_traffic_launch("prefill.cu", name))},
+                                                  + str(_traffic_launch(kfile, name))},
                      "store_ms": round(t_st, 4), "store_gbs": round(store_bytes / (t_st * 1e-3) / 1e9, 1),
                      "l2": "256 MB buffer written, then another 256 MB read, between launches",
                      "queue": "launches queued behind a device-side sleep, so the events time the kernels, "
@@ -711,7 +740,7 @@ def run_f16(pkv, args, dev, hbm_peak, bf16_peak):
     if pkv.pkv_device_error():
         raise RuntimeError("device error word set by the fp16 decode")
     res = {"decode": {"workload": "batched_decode_b256_ctx512-4096 (fp16)", "avg_launch_ms": round(dec_ms, 5),
-                      "roofline": {"kernel": "decode_split_kernel<fp16>", "bound": "hbm", "achieved": round(ach, 1),
+                      "roofline": {"kernel": _decode_kernel(c["B"]) + "<fp16>", "bound": "hbm", "achieved": round(ach, 1),
                                    "peak": hbm_peak, "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
                                    "traffic": None}}}
     del c
