@@ -409,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_persistent_kernel(const De
   float* pbuf = reinterpret_cast<float*>(qbuf + 2 * kQRowBytes);                 // [8 warps][kN]
   int4* hdr = reinterpret_cast<int4*>(pbuf + kConsumerWarps * kN);               // one per stage
   uint64_t* bars = reinterpret_cast<uint64_t*>(hdr + kStages);                   // full, empty, qfree[2]
-  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);                    // 32 ints
-  int* sF = misc + 32;                                                           // [B + 1]
+  int* misc = reinterpret_cast<int*>(bars + 2 * kStages + 2);                    // 96 ints
+  int* sF = misc + 96;                                                           // [B + 1]
   int* plist = sF + kPersistMaxSeqs + 1;                                         // [B]
 
   const int tid = threadIdx.x;
@@ -425,88 +425,109 @@ __global__ void __launch_bounds__(kThreads, 2) decode_persistent_kernel(const De
   const uint32_t qfree0 = empty0 + 8 * kStages;
 
   // ---- item tables ----
-  // sF[b] first holds the checked context length; padding rows and rows with
-  // a bad length have none and get zeros (written by the CTA with b % G == cta).
-  for (int b = tid; b < B; b += kThreads) {
-    int ctx = p.context_lens[b];
-    if (ctx < 0 || ctx > p.max_ctx || ctx > p.bt_stride * kBlockSize) {
-      if (b % G == cta) flag_error(p.err, PKV_DEVERR_BAD_SEQLEN);
-      ctx = 0;
-    }
-    sF[b] = ctx;
-  }
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kConsumerWarps);
-    }
-    mbar_init(qfree0, kConsumerWarps);
-    mbar_init(qfree0 + 8, kConsumerWarps);
-    mbar_fence_init();
-  }
-  __syncthreads();
-  for (int b = cta; b < B; b += G) {
-    if (sF[b] == 0) {
-      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(b) * kHq * kHeadDim);
-      for (int i = tid; i < kHq * kHeadDim / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  // partial chunks by size class: warp w counts class w (sizes 256-32(w+1) .. 255-32w)
-  auto size_class = [&](int b) -> int {
-    if (b >= B) return -1;
-    const int part = sF[b] & (kBlockSize - 1);
+  // Warps 0..7 each take a slice of 64 sequences (two rounds of 32 lanes),
+  // the context lengths held in registers. Pass 1 counts whole chunks and
+  // partial chunks per size class; pass 2 writes each sequence's whole-chunk
+  // prefix into sF and each partial chunk's sequence into plist, at its
+  // class's place. Rows with a bad length count as padding (no items); the
+  // producer warp writes the zeros of padding rows (rows b with b % G == cta)
+  // and initialises the barriers meanwhile.
+  static_assert(kPersistMaxSeqs == kConsumerWarps * 64, "two 32-lane rounds per slice");
+  int* cnt = misc + 32;  // [8 warps][8 classes]
+  int ctxv[2] = {0, 0};
+  auto size_class = [](int ctx) -> int {
+    const int part = ctx & (kBlockSize - 1);
     return part ? (kBuckets - 1) - (part >> 5) : -1;
   };
-  if (warp < kBuckets) {
-    int cnt = 0;
-    for (int base = 0; base < B; base += 32) cnt += __popc(__ballot_sync(0xffffffffu, size_class(base + lane) == warp));
-    if (lane == 0) misc[8 + warp] = cnt;
-  }
-  __syncthreads();
-  if (warp < kBuckets) {
-    int run = 0;
-    for (int w = 0; w < warp; ++w) run += misc[8 + w];
-    const uint32_t below = (1u << lane) - 1u;
-    for (int base = 0; base < B; base += 32) {
-      const int b = base + lane;
-      const uint32_t m = __ballot_sync(0xffffffffu, size_class(b) == warp);
-      if (size_class(b) == warp) plist[run + __popc(m & below)] = b;
-      run += __popc(m);
-    }
-  }
-  __syncthreads();
-  // exclusive prefix of the whole-chunk counts (threads 0..255, 2 sequences each)
-  {
-    int v0 = 0, v1 = 0;
-    const int b0 = 2 * tid;
-    if (tid < 256) {
-      v0 = b0 < B ? (sF[b0] >> 8) : 0;
-      v1 = b0 + 1 < B ? (sF[b0 + 1] >> 8) : 0;
-    }
-    int x = v0 + v1;  // inclusive warp scan of the pair sums
+  if (warp < kConsumerWarps) {
+    int full = 0;
+    int mycnt = 0;  // lane k < 8: partial chunks of class k in this slice
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, off);
-      if (lane >= off) x += y;
+    for (int r = 0; r < 2; ++r) {
+      const int b = warp * 64 + r * 32 + lane;
+      int ctx = b < B ? p.context_lens[b] : 0;
+      if (ctx < 0 || ctx > p.max_ctx || ctx > p.bt_stride * kBlockSize) {
+        if (b % G == cta) flag_error(p.err, PKV_DEVERR_BAD_SEQLEN);
+        ctx = 0;
+      }
+      ctxv[r] = ctx;
+      full += ctx >> 8;
+      const int cl = size_class(ctx);
+#pragma unroll
+      for (int k = 0; k < kBuckets; ++k) {
+        const int c = __popc(__ballot_sync(0xffffffffu, cl == k));
+        if (lane == k) mycnt += c;
+      }
     }
-    __syncthreads();  // every thread has read its sF entries
-    if (lane == 31 && warp < 8) misc[16 + warp] = x;
-    __syncthreads();
-    int before = 0;
-    for (int w = 0; w < warp && w < 8; ++w) before += misc[16 + w];
-    if (tid < 256) {
-      const int excl = before + x - (v0 + v1);
-      if (b0 < B) sF[b0] = excl;
-      if (b0 + 1 < B) sF[b0 + 1] = excl + v0;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) full += __shfl_xor_sync(0xffffffffu, full, off);
+    if (lane == 0) misc[16 + warp] = full;
+    if (lane < kBuckets) cnt[warp * kBuckets + lane] = mycnt;
+  } else {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(full0 + 8 * s, 1);
+        mbar_init(empty0 + 8 * s, kConsumerWarps);
+      }
+      mbar_init(qfree0, kConsumerWarps);
+      mbar_init(qfree0 + 8, kConsumerWarps);
+      mbar_fence_init();
+    }
+    for (int b = cta; b < B; b += G) {
+      const int ctx = p.context_lens[b];
+      if (ctx <= 0 || ctx > p.max_ctx || ctx > p.bt_stride * kBlockSize) {
+        uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(b) * kHq * kHeadDim);
+        for (int i = lane; i < kHq * kHeadDim / 8; i += 32) o[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp < kConsumerWarps) {
+    int run = 0, n_full_all = 0;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const int f = misc[16 + w];
+      if (w < warp) run += f;
+      n_full_all += f;
+    }
+    // lane k < 8: where this slice's class-k partial chunks go in plist
+    int cbase = 0, n_part_all = 0;
+    for (int k = 0; k < kBuckets; ++k) {
+      int tot = 0, before = 0;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const int c = cnt[w * kBuckets + k];
+        tot += c;
+        if (w < warp) before += c;
+      }
+      if (k < lane) cbase += tot;
+      if (k == lane) cbase += before;
+      n_part_all += tot;
+    }
+    const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int b = warp * 64 + r * 32 + lane;
+      const int nf = ctxv[r] >> 8;
+      int x = nf;  // inclusive scan over the round
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+      }
+      if (b < B) sF[b] = run + x - nf;
+      run += __shfl_sync(0xffffffffu, x, 31);
+      const int cl = size_class(ctxv[r]);
+#pragma unroll
+      for (int k = 0; k < kBuckets; ++k) {
+        const uint32_t m = __ballot_sync(0xffffffffu, cl == k);
+        const int base_k = __shfl_sync(0xffffffffu, cbase, k);
+        if (cl == k) plist[base_k + __popc(m & below)] = b;
+        if (lane == k) cbase += __popc(m);
+      }
     }
     if (tid == 0) {
-      int tot = 0;
-      for (int w = 0; w < 8; ++w) tot += misc[16 + w];
-      sF[B] = tot;
-      misc[1] = tot;  // whole chunks
-      int parts = 0;
-      for (int w = 0; w < kBuckets; ++w) parts += misc[8 + w];
-      misc[2] = tot + parts;  // all items
+      sF[B] = n_full_all;
+      misc[1] = n_full_all;               // whole chunks
+      misc[2] = n_full_all + n_part_all;  // all items
     }
   }
   __syncthreads();
@@ -827,7 +848,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t persistent_smem_bytes() {
   return static_cast<size_t>(kDecStages) * 2 * kDecT * kRowBytes + 2 * kQRowBytes +
          kConsumerWarps * 2 * kDecT * sizeof(float) + kDecStages * sizeof(int4) + (2 * kDecStages + 2) * sizeof(uint64_t) +
-         32 * sizeof(int) + (2 * kPersistMaxSeqs + 1) * sizeof(int);
+         96 * sizeof(int) + (2 * kPersistMaxSeqs + 1) * sizeof(int);
 }
 static_assert(2 * (persistent_smem_bytes() + 1024) <= 228 * 1024, "two persistent decode CTAs must fit an SM");
 
