@@ -570,6 +570,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_pv(0, rv % kKvSlots, first);
           mma_commit(bar(kBarOFinal + 0));
+          // Both groups' last P.V go before the next unit's S products: the
+          // epilogues start as early as possible, and the next unit's Q and
+          // K_0, still in flight, hold up no product of this unit.
+          if (!(ok = wait_or_abort(bar(kBarPReady + 1), t & 1, s_abort, p.err))) break;
+          if (first && nu > 0 && !(ok = wait_or_abort(bar(kBarOFree + 1), (nu - 1) & 1, s_abort, p.err))) break;
+          tc_fence_after();
+          issue_pv(1, rv % kKvSlots, first);
+          mma_commit(bar(kBarKvFree + rv % kKvSlots));
+          mma_commit(bar(kBarOFinal + 1));
           const Unit nxt = read_desc(d++);
           if (!(ok = nxt.valid != -2)) break;
           mbar_arrive(bar(kBarDescFree + (d - 1) % kDescSlots));
@@ -580,14 +589,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             issue_s(0, rk % kKvSlots);
             mma_commit(bar(kBarSFull + 0));
-          }
-          if (!(ok = wait_or_abort(bar(kBarPReady + 1), t & 1, s_abort, p.err))) break;
-          if (first && nu > 0 && !(ok = wait_or_abort(bar(kBarOFree + 1), (nu - 1) & 1, s_abort, p.err))) break;
-          tc_fence_after();
-          issue_pv(1, rv % kKvSlots, first);
-          mma_commit(bar(kBarKvFree + rv % kKvSlots));
-          mma_commit(bar(kBarOFinal + 1));
-          if (more) {
             issue_s(1, rk % kKvSlots);
             mma_commit(bar(kBarSFull + 1));
             mma_commit(bar(kBarKvFree + rk % kKvSlots));
