@@ -118,6 +118,69 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
   return v[0];
 }
 
+// Split-KV merge of sequence b's nch partials (m, l, o) for query head hq,
+// dims d0..d0+7 (one thread), written to the output row:
+//   o = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,  M = max_c m_c.
+// The partials sit in L2 (other CTAs wrote them), so the merge is bound by
+// round trips: it reads them four chunks at a time, every load of a group in
+// flight together, and keeps a running maximum (rescaling what it has summed
+// when the maximum grows), one pass over the chunks.
+template <Elem E>
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, int b, int nch, int hq, int d0) {
+  using Ops = ElemOps<E>;
+  constexpr int kG = 4;
+  const int64_t base = static_cast<int64_t>(b) * p.nsplit * kHq + hq;
+  float M = -INFINITY, den = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int c0 = 0; c0 < nch; c0 += kG) {
+    float2 ml[kG];
+    float4 x[kG], y[kG];
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      if (c0 + j < nch) {
+        const int64_t slot = base + static_cast<int64_t>(c0 + j) * kHq;
+        ml[j] = __ldcg(p.ml + slot);
+        x[j] = __ldcg(reinterpret_cast<const float4*>(p.opart + slot * kHeadDim + d0));
+        y[j] = __ldcg(reinterpret_cast<const float4*>(p.opart + slot * kHeadDim + d0 + 4));
+      } else {
+        ml[j] = make_float2(-INFINITY, 0.f);
+        x[j] = y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mg = M;
+#pragma unroll
+    for (int j = 0; j < kG; ++j) Mg = fmaxf(Mg, ml[j].x);
+    if (Mg > M) {
+      const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - Mg);
+      den *= sc;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] *= sc;
+      M = Mg;
+    }
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+#pragma unroll
+    for (int j = 0; j < kG; ++j) {
+      const float w = ex2_approx(ml[j].x - Mu);
+      den = fmaf(w, ml[j].y, den);
+      acc[0] = fmaf(w, x[j].x, acc[0]);
+      acc[1] = fmaf(w, x[j].y, acc[1]);
+      acc[2] = fmaf(w, x[j].z, acc[2]);
+      acc[3] = fmaf(w, x[j].w, acc[3]);
+      acc[4] = fmaf(w, y[j].x, acc[4]);
+      acc[5] = fmaf(w, y[j].y, acc[5]);
+      acc[6] = fmaf(w, y[j].z, acc[6]);
+      acc[7] = fmaf(w, y[j].w, acc[7]);
+    }
+  }
+  const float r = den > 0.f ? 1.f / den : 0.f;
+  uint4 w;
+  w.x = Ops::pack(acc[0] * r, acc[1] * r);
+  w.y = Ops::pack(acc[2] * r, acc[3] * r);
+  w.z = Ops::pack(acc[4] * r, acc[5] * r);
+  w.w = Ops::pack(acc[6] * r, acc[7] * r);
+  *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + hq) * kHeadDim + d0) = w;
+}
+
 template <Elem E, int kT, int kStages>
 __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100 * 1024) ? 2 : 1)
     decode_split_kernel(const DecodeParams p) {
@@ -338,39 +401,7 @@ __global__ void __launch_bounds__(kThreads, (kStages * 2 * kT * kRowBytes <= 100
   __syncthreads();
   if (*s_last == 0) return;
   __threadfence();
-  if (threadIdx.x < kHq * 16) {
-    const int hq = threadIdx.x >> 4;
-    const int d0 = (threadIdx.x & 15) * 8;
-    const int64_t base = static_cast<int64_t>(b) * p.nsplit * kHq + hq;
-    float M = -INFINITY;
-    for (int cc = 0; cc < nchunks; ++cc) M = fmaxf(M, __ldcg(p.ml + base + static_cast<int64_t>(cc) * kHq).x);
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float den = 0.f;
-    for (int cc = 0; cc < nchunks; ++cc) {
-      const int64_t slot = base + static_cast<int64_t>(cc) * kHq;
-      const float2 ml = __ldcg(p.ml + slot);
-      const float w = ex2_approx(ml.x - Mu);
-      den = fmaf(w, ml.y, den);
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(p.opart + slot * kHeadDim + d0));
-      const float4 y = __ldcg(reinterpret_cast<const float4*>(p.opart + slot * kHeadDim + d0 + 4));
-      acc[0] = fmaf(w, x.x, acc[0]);
-      acc[1] = fmaf(w, x.y, acc[1]);
-      acc[2] = fmaf(w, x.z, acc[2]);
-      acc[3] = fmaf(w, x.w, acc[3]);
-      acc[4] = fmaf(w, y.x, acc[4]);
-      acc[5] = fmaf(w, y.y, acc[5]);
-      acc[6] = fmaf(w, y.z, acc[6]);
-      acc[7] = fmaf(w, y.w, acc[7]);
-    }
-    const float r = den > 0.f ? 1.f / den : 0.f;
-    uint4 w;
-    w.x = Ops::pack(acc[0] * r, acc[1] * r);
-    w.y = Ops::pack(acc[2] * r, acc[3] * r);
-    w.z = Ops::pack(acc[4] * r, acc[5] * r);
-    w.w = Ops::pack(acc[6] * r, acc[7] * r);
-    *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + hq) * kHeadDim + d0) = w;
-  }
+  if (threadIdx.x < kHq * 16) merge_partials<E>(p, b, nchunks, threadIdx.x >> 4, (threadIdx.x & 15) * 8);
   if (threadIdx.x == 0) p.tickets[b] = 0;  // ready for the next call
 }
 
@@ -798,39 +829,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_persistent_kernel(const De
     named_sync_consumers();
     if (*s_last == 0) continue;
     __threadfence();
-    {
-      const int hq = tid >> 4;
-      const int d0 = (tid & 15) * 8;
-      const int64_t base = static_cast<int64_t>(b) * p.nsplit * kHq + hq;
-      float M = -INFINITY;
-      for (int cc = 0; cc < nch; ++cc) M = fmaxf(M, __ldcg(p.ml + base + static_cast<int64_t>(cc) * kHq).x);
-      const float Mu = (M == -INFINITY) ? 0.f : M;
-      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      float den = 0.f;
-      for (int cc = 0; cc < nch; ++cc) {
-        const int64_t sl = base + static_cast<int64_t>(cc) * kHq;
-        const float2 ml = __ldcg(p.ml + sl);
-        const float w = ex2_approx(ml.x - Mu);
-        den = fmaf(w, ml.y, den);
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(p.opart + sl * kHeadDim + d0));
-        const float4 y = __ldcg(reinterpret_cast<const float4*>(p.opart + sl * kHeadDim + d0 + 4));
-        acc[0] = fmaf(w, x.x, acc[0]);
-        acc[1] = fmaf(w, x.y, acc[1]);
-        acc[2] = fmaf(w, x.z, acc[2]);
-        acc[3] = fmaf(w, x.w, acc[3]);
-        acc[4] = fmaf(w, y.x, acc[4]);
-        acc[5] = fmaf(w, y.y, acc[5]);
-        acc[6] = fmaf(w, y.z, acc[6]);
-        acc[7] = fmaf(w, y.w, acc[7]);
-      }
-      const float r = den > 0.f ? 1.f / den : 0.f;
-      uint4 w;
-      w.x = Ops::pack(acc[0] * r, acc[1] * r);
-      w.y = Ops::pack(acc[2] * r, acc[3] * r);
-      w.z = Ops::pack(acc[4] * r, acc[5] * r);
-      w.w = Ops::pack(acc[6] * r, acc[7] * r);
-      *reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(b) * kHq + hq) * kHeadDim + d0) = w;
-    }
+    merge_partials<E>(p, b, nch, tid >> 4, (tid & 15) * 8);
     if (tid == 0) p.tickets[b] = 0;  // ready for the next call
   }
 }
