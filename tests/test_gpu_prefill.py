@@ -331,3 +331,23 @@ def test_plan_naming_missing_sequences_is_flagged(pkv):
                                  block_tables=to_dev(meta["block_tables"], dev))
     torch.cuda.synchronize()
     assert torch.equal(out, ref)          # the one real sequence is complete
+
+
+def test_longest_prompt_and_context(pkv):
+    """A single prompt at max_model_len (4096 tokens, 32 query tiles of up to 32
+    key tiles, poisoned pool, keys also from contiguous k/v), then 96 new tokens
+    at the end of a 4096-token context; sampled rows, the last rows included."""
+    rng = np.random.default_rng(71)
+    seqs, nb = _seqs_with_tables([(0, W.MAX_MODEL_LEN)], rng)
+    meta_q = np.array([0, W.MAX_MODEL_LEN])
+    _run(pkv, seqs, nb, 71, poison=True, sample_rows=_rows_sample(meta_q, rng, per_seq=24), check_contiguous=True)
+    seqs, nb = _seqs_with_tables([(W.MAX_MODEL_LEN - 96, 96)], rng)
+    _run(pkv, seqs, nb, 72, poison=True)
+
+
+def test_sequence_without_new_tokens(pkv):
+    """A sequence whose tokens are all cached (no query rows this call) between
+    two that have some: it gets no rows, and the others are unaffected."""
+    rng = np.random.default_rng(73)
+    seqs, nb = _seqs_with_tables([(300, 5), (256, 0), (0, 77), (0, 0), (513, 140)], rng)
+    _run(pkv, seqs, nb, 73, poison=True)
