@@ -294,3 +294,15 @@ def test_f16_and_bf16_see_the_same_values(pkv):
     diff = (outs[torch.bfloat16] - outs[torch.float16]).abs()
     assert float(diff.max()) <= 2.0 ** -8 * 2.0 + 1e-6       # one bf16 ulp of |o| <= 2, plus fp16 rounding
     assert pkv.pkv_device_error() == 0
+
+
+def test_many_sequences_grid_rows(pkv):
+    """3,000 sequences of 1..600 tokens (grid form, 3,000 rows of CTAs along
+    the second grid dimension, two to three splits each): sampled rows from the
+    first, last and middle sequences against the oracle."""
+    rng = np.random.default_rng(99)
+    ctxs = [int(x) for x in rng.integers(1, 601, size=3000)]
+    nb = sum(W.blocks_for(c) for c in ctxs) + 4
+    wl = W.Workload("many_seqs", 99, W._decode_seqs(ctxs, nb, rng), nb, "decode")
+    sample = sorted({0, 1, 1499, 1500, 2998, 2999, *rng.choice(3000, 6, replace=False).tolist()})
+    _decode_step(pkv, wl, "cuda", sample=sample, poison=True)
